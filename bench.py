@@ -1,0 +1,457 @@
+"""Benchmark of the tree-verify step on GB300.
+
+One step = one verify round over one batch of synthetic input: tree mask,
+split-KV tree attention + merge, per-node argmax, acceptance walk and the
+accept(k) commit (five launches of this library's kernels), plus a reset of
+prefix_len so that every step verifies the same workload.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5] [--impl ours|reference]
+
+Prints one JSON line.  `value` = verified query rows (tree nodes) per second
+over the whole job, inputs resident in HBM, measured with CUDA events around
+K CUDA-graph replays; between steps the inputs rotate over enough copies that
+each step reads them from HBM, not L2.  `e2e` = the same metric through the
+public Python API with pinned host inputs copied in and the results copied
+out every step.  `roofline` = the split-KV attention kernel's algorithmic
+bytes per launch over its CUDA-event duration, against the measured HBM
+copy bandwidth.  `cpu_baseline` = the float64 oracle on the host cores.
+With --impl reference the oracle itself is timed as the reference arm.
+"""
+from __future__ import annotations
+
+import os
+import sys
+
+_CORES = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, str(_CORES))
+
+import argparse
+import hashlib
+import json
+import math
+import statistics
+import subprocess
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from speculative_decoding_tree_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "tree-verify attention: query rows/s and HBM GB/s vs peak; accept+commit µs"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", type=int, default=4, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- helpers
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return ws, rank
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    csrc = os.path.join(ROOT, "speculative_decoding_tree_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload_name):
+    """dram bytes per launch of the split kernel from the committed ncu summary,
+    only while the kernel sources are unchanged since the capture."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d.get(workload_name)
+        if e and e.get("source_hash") == kernel_source_hash():
+            return e.get("bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- workloads
+
+def make_sets(spec, device):
+    """Enough independent copies of the workload that a step's inputs are not
+    in L2 when it starts (rotating over them)."""
+    from speculative_decoding_tree_gb300.runner import DeviceStep
+
+    def argmax_cpu(x):          # only to plant draft matches in the synthetic input
+        return torch.argmax(x.float(), dim=1)
+
+    sets = []
+    w0 = wl.make_workload(spec, canary=0.0, argmax_fn=argmax_cpu)
+    per_set = (w0.k_cache.numel() * w0.k_cache.element_size() * 2 + w0.logits.numel() * w0.logits.element_size()
+               + w0.q.numel() * w0.q.element_size() * 2)
+    nsets = max(2, math.ceil(3 * L2_BYTES / per_set))
+    for i in range(nsets):
+        w = w0 if i == 0 else wl.make_workload(spec.replace(seed=spec.seed + 7919 * i), canary=0.0,
+                                               argmax_fn=argmax_cpu)
+        st = DeviceStep(w, device=device)
+        st.p0 = st.prefix_len.clone()
+        sets.append(st)
+    return sets, per_set
+
+
+def algorithmic_bytes(w):
+    """Per verify step, from the workload itself: attention = every K/V
+    element of prefix and tree once + Q + O; split kernel = K/V + Q; accept
+    = the logits once + 2x the committed K/V rows."""
+    sp = w.spec
+    es = 4 if sp.dtype == "f32" else 2
+    les = 4 if sp.logit_dtype == "f32" else 2
+    kv = q = o = 0
+    for b in range(sp.batch):
+        P = int(w.prefix_len[b])
+        n = len(w.parents[b])
+        kv += (P + n) * sp.hkv * sp.d * 2 * es
+        q += n * sp.hq * sp.d * es
+        o += n * sp.hq * sp.d * es
+    logits = w.total_rows * sp.vocab * les
+    return dict(kv=kv, q=q, o=o, attn=kv + q + o, split=kv + q, logits=logits)
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, ws, rank):
+    import numpy as np  # noqa: F401
+    from speculative_decoding_tree_gb300 import _build
+    _build.build()
+    import speculative_decoding_tree_gb300 as tv
+
+    device = torch.device("cuda", torch.cuda.current_device())
+    spec = wl.CONFIGS[args.config]
+    sets, per_set = make_sets(spec, device)
+    nsets = len(sets)
+    w = sets[0].w
+    rows = w.total_rows
+    stream = torch.cuda.current_stream()
+
+    def step(st):
+        st.prefix_len.copy_(st.p0, non_blocking=True)
+        st.step()
+
+    # warm-up (eager), then one CUDA graph per input set
+    for i in range(max(args.warmup, 3)):
+        step(sets[i % nsets])
+    torch.cuda.synchronize()
+    graphs = []
+    cap_stream = torch.cuda.Stream()
+    for st in sets:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap_stream):
+            step(st)
+        graphs.append(g)
+    for i in range(max(args.warmup, 3)):
+        graphs[i % nsets].replay()
+    torch.cuda.synchronize()
+    for st in sets:
+        st.status.zero_()
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    # settle the clocks under load (untimed), then the timed region
+    t_end = time.time() + 1.0
+    i = 0
+    while time.time() < t_end:
+        graphs[i % nsets].replay()
+        i += 1
+        if i % 64 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    barrier(ws)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(10_000_000)        # let the queue run ahead of the GPU
+    ev0.record()
+    for i in range(args.steps):
+        graphs[i % nsets].replay()
+    ev1.record()
+    torch.cuda.synchronize()
+    barrier(ws)
+    torch.cuda.synchronize()
+    elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), ws)
+
+    # per-kernel durations: eager steps with events around each call, the
+    # queue pre-filled so launches do not wait on the host
+    n_k = min(args.steps, 200)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n_k)]
+    torch.cuda.synchronize()
+    torch.cuda._sleep(80_000_000)
+    for i in range(n_k):
+        st = sets[i % nsets]
+        e = evs[i]
+        st.prefix_len.copy_(st.p0, non_blocking=True)
+        e[0].record()
+        st.mask()
+        e[1].record()
+        st.partials()
+        e[2].record()
+        st.merge()
+        e[3].record()
+        st.accept_commit()
+        e[4].record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    mask_us = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) * 1e3
+    split_us = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) * 1e3
+    merge_us = statistics.mean(e[2].elapsed_time(e[3]) for e in evs) * 1e3
+    acc_us = statistics.mean(e[3].elapsed_time(e[4]) for e in evs) * 1e3
+    status = sum(int(st.status[0].item()) for st in sets)
+
+    # e2e through the public API with host buffers: per step copy the step's
+    # inputs in from pinned memory, run the step, copy the results out
+    st = sets[0]
+    host_in = {k: getattr(st, k).cpu().pin_memory() for k in
+               ("q", "k_tree", "v_tree", "logits", "draft", "parents", "node_offsets")}
+    host_out = {k: torch.empty_like(getattr(st, k), device="cpu").pin_memory() for k in
+                ("accept_len", "tokens", "path")}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    n_e2e = min(args.steps, 50)
+    for rep in range(2):
+        torch.cuda.synchronize()
+        barrier(ws)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(n_e2e):
+            for k, t in host_in.items():
+                getattr(st, k).copy_(t, non_blocking=True)
+            st.prefix_len.copy_(st.p0, non_blocking=True)
+            st.step()
+            for k, t in host_out.items():
+                t.copy_(getattr(st, k), non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws)
+
+    ab = algorithmic_bytes(w)
+    peak, peak_kind = measured_peaks()
+    ms_per_step = elapsed_ms / args.steps
+    value = ws * rows * args.steps / (elapsed_ms / 1e3)
+    plan = tv.tv_attn_plan(st.desc)
+    achieved = ab["split"] / (split_us * 1e-6) / 1e9
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": "rows/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype, "data": "synthetic",
+        "config": {
+            "workload": spec.name, "batch": spec.batch, "q_heads": spec.hq, "kv_heads": spec.hkv,
+            "head_dim": spec.d, "prefix": list(spec.prefix), "tree_rows": rows, "vocab": spec.vocab,
+            "paged": spec.paged, "parallelism": "replicas" if ws > 1 else "single",
+            "l2": f"inputs rotate over {nsets} copies ({nsets * per_set / 1e6:.0f} MB > 129 MB L2)",
+            "timing": "CUDA-graph replays of whole steps, CUDA events",
+        },
+        "roofline": {
+            "kernel": "tv_attn_tc_kernel" if plan["kernel"] == 1 else "attn_simt_kernel",
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+            "traffic": profiled_traffic(spec.name),
+            "algorithmic_bytes_per_launch": ab["split"],
+        },
+        "e2e": {"value": round(ws * rows * n_e2e / (e2e_ms / 1e3), 1), "unit": "rows/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": st.KERNELS_PER_STEP * args.steps,
+        "clocks": clocks,
+        "breakdown_us": {"mask": round(mask_us, 2), "attn_split": round(split_us, 2),
+                         "attn_merge": round(merge_us, 2), "accept_commit": round(acc_us, 2)},
+        "attn_call": {"gbs": round(ab["attn"] / ((split_us + merge_us) * 1e-6) / 1e9, 1),
+                      "frac": round(ab["attn"] / ((split_us + merge_us) * 1e-6) / 1e9 / peak, 4),
+                      "algorithmic_bytes": ab["attn"]},
+        "accept_commit_us": round(acc_us, 2),
+        "plan": plan,
+        "device_status": status,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(spec, args.cpu_seconds)
+    return res
+
+
+# ---------------------------------------------------------------- oracle arms
+
+def oracle_sample_step(w, rows):
+    """The oracle on a bounded sample: attention for the first `rows` tree
+    rows (all heads), their argmax, and acceptance + commit of every sequence."""
+    import oracle
+    import numpy as np
+    samples = [(r, h) for r in range(rows) for h in range(w.spec.hq)]
+    oracle.tree_attention(w, samples)
+    am = np.zeros(w.total_rows, dtype=np.int64)
+    am[:rows] = oracle.argmax_rows(w.logits[:rows])
+    acc = []
+    for b in range(w.batch):
+        o0, o1 = w.seq_rows(b)
+        acc.append(oracle.accept(w.parents[b], w.draft_tokens[o0:o1].tolist(), am[o0:o1].tolist()))
+    oracle.commit(w, acc)
+
+
+def _oracle_workload(spec):
+    import oracle
+    return wl.make_workload(spec, canary=0.0, argmax_fn=oracle.argmax_rows)
+
+
+def cpu_baseline(spec, seconds):
+    w = _oracle_workload(spec)
+    t = time.perf_counter()
+    oracle_sample_step(w, 1)
+    one = max(time.perf_counter() - t, 1e-4)
+    rows = max(1, min(w.total_rows, int(seconds / one)))
+    t = time.perf_counter()
+    oracle_sample_step(w, rows)
+    dt = time.perf_counter() - t
+    return {"value": round(rows / dt, 3), "unit": "rows/s", "cores": _CORES, "kind": "oracle",
+            "sample": f"{rows} of {w.total_rows} tree rows (all {spec.hq} heads, float64 attention), their "
+                      f"argmax, acceptance and commit; {dt:.1f} s; cores = BLAS/OpenMP thread cap"}
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return None
+    spec = wl.CONFIGS[args.config]
+    w = _oracle_workload(spec)
+    t = time.perf_counter()
+    oracle_sample_step(w, 1)
+    one = max(time.perf_counter() - t, 1e-4)
+    budget = 90.0 / max(1, args.steps + args.warmup)
+    rows = max(1, min(w.total_rows, int(budget / one)))
+    for _ in range(args.warmup):
+        oracle_sample_step(w, rows)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_sample_step(w, rows)
+    dt = time.perf_counter() - t
+    value = rows * args.steps / dt
+    sample = (f"each step: {rows} of {w.total_rows} tree rows (all heads) through the float64 oracle, "
+              f"their argmax, acceptance and commit")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "rows/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": spec.name, "batch": spec.batch, "q_heads": spec.hq, "kv_heads": spec.hkv,
+                   "head_dim": spec.d, "prefix": list(spec.prefix), "vocab": spec.vocab},
+        "cpu_baseline": {"value": round(value, 3), "unit": "rows/s", "cores": _CORES, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        ws = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        res = run_reference(args, ws, rank)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    ws, rank = dist_setup()
+    res = run_ours(args, ws, rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,1 +1,168 @@
-"""Tree-verify step for tree speculative decoding on GB300 (sm_103a)."""
+"""Tree-verify step of tree speculative decoding on GB300 (sm_103a).
+
+A thin ctypes binding over libtreeverify.so, whose C ABI is declared in
+include/tree_verify.h.  Every function here only marshals arguments (torch
+tensors or raw device addresses, a stream) and raises on a non-zero status;
+all work happens in the library's CUDA kernels.  There is no CPU fallback:
+calling into a library that was not built raises ``LibraryNotBuilt``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "TvDesc", "TvPlan", "TreeVerifyError", "LibraryNotBuilt", "F32", "BF16", "DEV_BITS",
+    "lib", "make_desc", "tv_workspace_size", "tv_attn_plan", "tv_status_string", "tv_version",
+    "tv_build_tree_mask", "tree_verify_attn", "tv_attn_partials", "tv_attn_merge", "tree_accept_commit",
+]
+
+F32, BF16 = 0, 1
+DEV_BITS = {1: "BAD_TREE", 2: "BAD_OFFSETS", 4: "BAD_PREFIX", 8: "BAD_PAGE", 16: "CAPACITY", 32: "TIMEOUT"}
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtreeverify.so")
+
+
+class LibraryNotBuilt(RuntimeError):
+    pass
+
+
+class TreeVerifyError(RuntimeError):
+    def __init__(self, code, where):
+        self.code = code
+        super().__init__(f"{where}: {tv_status_string(code)} ({code})")
+
+
+class TvDesc(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int32), ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32), ("out_f32", ctypes.c_int32),
+        ("scale", ctypes.c_float), ("max_nodes", ctypes.c_int32), ("total_rows", ctypes.c_int32),
+        ("page_size", ctypes.c_int32), ("capacity", ctypes.c_int64), ("num_pages", ctypes.c_int64),
+        ("max_prefix", ctypes.c_int64),
+    ]
+
+
+class TvPlan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("kernel", "num_splits", "chunk", "row_tiles", "rows_per_tile", "grid_ctas")]
+
+
+_LIB = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int32
+_SIG = {
+    "tv_workspace_size": [ctypes.POINTER(TvDesc), _I, ctypes.POINTER(ctypes.c_size_t)],
+    "tv_attn_plan": [ctypes.POINTER(TvDesc), ctypes.POINTER(TvPlan)],
+    "tv_build_tree_mask": [ctypes.POINTER(TvDesc), _P, _P, _P, _P, _P, _P],
+    "tree_verify_attn": [ctypes.POINTER(TvDesc)] + [_P] * 11 + [ctypes.c_size_t, _P, _P],
+    "tv_attn_partials": [ctypes.POINTER(TvDesc)] + [_P] * 10 + [ctypes.c_size_t, _P, _P],
+    "tv_attn_merge": [ctypes.POINTER(TvDesc), _P, _P, _P, _P, ctypes.c_size_t, _P, _P],
+    "tree_accept_commit": [ctypes.POINTER(TvDesc), _I, _I] + [_P] * 15 + [ctypes.c_size_t, _P, _P],
+}
+
+
+def lib(path: str = LIB_PATH):
+    """The loaded library (loaded on first use)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(path):
+            raise LibraryNotBuilt(
+                f"{path} is missing: build it with speculative_decoding_tree_gb300._build.build() "
+                "(the tree-verify step has no CPU fallback)")
+        L = ctypes.CDLL(path)
+        for name, args in _SIG.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        L.tv_status_string.argtypes = [ctypes.c_int]
+        L.tv_status_string.restype = ctypes.c_char_p
+        L.tv_version.argtypes = []
+        L.tv_version.restype = ctypes.c_char_p
+        _LIB = L
+    return _LIB
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(rc, where):
+    if rc != 0:
+        raise TreeVerifyError(rc, where)
+
+
+def make_desc(*, batch, num_q_heads, num_kv_heads, head_dim, dtype, max_nodes, total_rows, capacity,
+              max_prefix, page_size=0, num_pages=0, out_f32=0, scale=0.0) -> TvDesc:
+    return TvDesc(batch, num_q_heads, num_kv_heads, head_dim, dtype, out_f32, scale, max_nodes, total_rows,
+                  page_size, capacity, num_pages, max_prefix)
+
+
+def tv_status_string(code: int) -> str:
+    return lib().tv_status_string(int(code)).decode()
+
+
+def tv_version() -> str:
+    return lib().tv_version().decode()
+
+
+def tv_workspace_size(desc: TvDesc, vocab: int = 0) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().tv_workspace_size(ctypes.byref(desc), int(vocab), ctypes.byref(n)), "tv_workspace_size")
+    return n.value
+
+
+def tv_attn_plan(desc: TvDesc) -> dict:
+    p = TvPlan()
+    _check(lib().tv_attn_plan(ctypes.byref(desc), ctypes.byref(p)), "tv_attn_plan")
+    return {name: getattr(p, name) for name, _ in TvPlan._fields_}
+
+
+def tv_build_tree_mask(desc, parents, node_offsets, anc, depth, status, stream=None):
+    _check(lib().tv_build_tree_mask(ctypes.byref(desc), _ptr(parents), _ptr(node_offsets), _ptr(anc),
+                                    _ptr(depth), _ptr(status), _stream(stream)), "tv_build_tree_mask")
+
+
+def tree_verify_attn(desc, q, k_cache, v_cache, page_table, prefix_len, node_offsets, k_tree, v_tree, anc, out,
+                     workspace, workspace_bytes, status, stream=None):
+    _check(lib().tree_verify_attn(ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table),
+                                  _ptr(prefix_len), _ptr(node_offsets), _ptr(k_tree), _ptr(v_tree), _ptr(anc),
+                                  _ptr(out), _ptr(workspace), int(workspace_bytes), _ptr(status),
+                                  _stream(stream)), "tree_verify_attn")
+
+
+def tv_attn_partials(desc, q, k_cache, v_cache, page_table, prefix_len, node_offsets, k_tree, v_tree, anc,
+                     workspace, workspace_bytes, status, stream=None):
+    _check(lib().tv_attn_partials(ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table),
+                                  _ptr(prefix_len), _ptr(node_offsets), _ptr(k_tree), _ptr(v_tree), _ptr(anc),
+                                  _ptr(workspace), int(workspace_bytes), _ptr(status), _stream(stream)),
+           "tv_attn_partials")
+
+
+def tv_attn_merge(desc, prefix_len, node_offsets, out, workspace, workspace_bytes, status, stream=None):
+    _check(lib().tv_attn_merge(ctypes.byref(desc), _ptr(prefix_len), _ptr(node_offsets), _ptr(out),
+                               _ptr(workspace), int(workspace_bytes), _ptr(status), _stream(stream)),
+           "tv_attn_merge")
+
+
+def tree_accept_commit(desc, vocab, logits_dtype, logits, draft_tokens, parents, node_offsets, k_tree, v_tree,
+                       k_cache, v_cache, page_table, prefix_len, argmax, accept_len, path, tokens, workspace,
+                       workspace_bytes, status, stream=None):
+    _check(lib().tree_accept_commit(ctypes.byref(desc), int(vocab), int(logits_dtype), _ptr(logits),
+                                    _ptr(draft_tokens), _ptr(parents), _ptr(node_offsets), _ptr(k_tree),
+                                    _ptr(v_tree), _ptr(k_cache), _ptr(v_cache), _ptr(page_table),
+                                    _ptr(prefix_len), _ptr(argmax), _ptr(accept_len), _ptr(path), _ptr(tokens),
+                                    _ptr(workspace), int(workspace_bytes), _ptr(status), _stream(stream)),
+           "tree_accept_commit")

@@ -1,0 +1,360 @@
+// Host side of the C ABI declared in include/tree_verify.h: descriptor
+// validation (all before any launch, with checked int64 arithmetic), the
+// split-KV launch plan, workspace carving, and the launches themselves.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "tv_internal.cuh"
+
+namespace tv {
+namespace {
+
+bool mul_ok(int64_t a, int64_t b, int64_t* out) { return !__builtin_mul_overflow(a, b, out); }
+bool add_ok(int64_t a, int64_t b, int64_t* out) { return !__builtin_add_overflow(a, b, out); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+int num_sms() {
+  static int cached = 0;
+  if (cached > 0) return cached;
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0) {
+    cached = n;
+  } else {
+    cudaGetLastError();  // clear the error left by a machine without a GPU
+    n = kNumSMsDefault;
+  }
+  return n;
+}
+
+// Checks shared by every entry point.  Order follows the pages' validation
+// list: dtype, head_dim, zero heads before the GQA modulo, shapes, overflow
+// ("ADR-037", phase rows E1 gate, E3 gate and E6 dispatcher).
+int validate(const tv_desc* d) {
+  if (!d) return TV_ERR_NULL;
+  if (d->dtype != TV_F32 && d->dtype != TV_BF16) return TV_ERR_DTYPE;
+  if (d->head_dim != 128 && d->head_dim != 256 && d->head_dim != 512) return TV_ERR_HEAD_DIM;
+  if (d->num_q_heads <= 0 || d->num_kv_heads <= 0) return TV_ERR_ZERO_HEADS;
+  if (d->num_q_heads % d->num_kv_heads != 0) return TV_ERR_GQA;
+  if (d->batch < 1) return TV_ERR_SHAPE;
+  if (d->max_nodes < 1 || d->max_nodes > kMaxNodes) return TV_ERR_TREE;
+  if (d->total_rows < d->batch || (int64_t)d->total_rows > (int64_t)d->batch * d->max_nodes) return TV_ERR_TREE;
+  if (!(std::isfinite(d->scale)) || d->scale < 0.f) return TV_ERR_SHAPE;
+  if (d->capacity < 1 || d->max_prefix < 0 || d->max_prefix > d->capacity) return TV_ERR_SHAPE;
+  if (d->page_size != 0 && d->page_size != kPageSize) return TV_ERR_PAGED;
+  if (d->page_size == kPageSize && (d->capacity % kPageSize != 0 || d->num_pages < 1)) return TV_ERR_PAGED;
+  // every element count the kernels index must fit int64 in bytes
+  int64_t esize = d->dtype == TV_BF16 ? 2 : 4, t = 0;
+  int64_t per_row = 0;
+  if (!mul_ok(d->head_dim, esize, &per_row)) return TV_ERR_OVERFLOW;
+  if (d->page_size == 0) {
+    if (!mul_ok(d->batch, d->num_kv_heads, &t) || !mul_ok(t, d->capacity, &t) || !mul_ok(t, per_row, &t))
+      return TV_ERR_OVERFLOW;
+  } else {
+    if (!mul_ok(d->num_pages, d->num_kv_heads, &t) || !mul_ok(t, kPageSize, &t) || !mul_ok(t, per_row, &t))
+      return TV_ERR_OVERFLOW;
+  }
+  if (!mul_ok(d->total_rows, d->num_q_heads, &t) || !mul_ok(t, per_row, &t)) return TV_ERR_OVERFLOW;
+  return TV_OK;
+}
+
+struct Plan {
+  tv_plan pub;
+  int G;
+  int64_t o_part_bytes, ml_part_bytes;
+};
+
+int make_plan(const tv_desc* d, Plan* p) {
+  int G = d->num_q_heads / d->num_kv_heads;
+  bool tc = d->dtype == TV_BF16 && d->max_nodes * G >= 16 && tc_supported(d->head_dim, G, d->dtype, d->max_nodes);
+  int key_tile = tc ? tc_key_tile(d->head_dim) : 32;
+  int rows_per_tile;
+  if (tc) {
+    rows_per_tile = (128 / G) * G;
+  } else {
+    int rpw = 1024 / d->head_dim;          // rows per warp in the CUDA-core kernel
+    rows_per_tile = 4 * rpw;
+  }
+  int row_tiles = (d->max_nodes * G + rows_per_tile - 1) / rows_per_tile;
+  int64_t units = (int64_t)d->batch * d->num_kv_heads * row_tiles;
+  int64_t sms = num_sms();
+  int64_t want = (sms * (d->batch > 1 ? 4 : 1)) / units;
+  if (want < 1) want = 1;
+  int64_t L = d->max_prefix;
+  int64_t chunk = (L + want - 1) / want;
+  chunk = align_up(chunk < 1 ? 1 : chunk, key_tile);
+  if (chunk > (int64_t)1 << 30) return TV_ERR_OVERFLOW;
+  int splits = num_chunks(L, (int)chunk);
+  int64_t grid = units * splits;
+  if (grid > ((int64_t)1 << 31) - 1) return TV_ERR_OVERFLOW;
+  p->G = G;
+  p->pub.kernel = tc ? 1 : 0;
+  p->pub.num_splits = splits;
+  p->pub.chunk = (int)chunk;
+  p->pub.row_tiles = row_tiles;
+  p->pub.rows_per_tile = rows_per_tile;
+  p->pub.grid_ctas = (int)grid;
+  int64_t t;
+  if (!mul_ok(splits, d->total_rows, &t) || !mul_ok(t, d->num_q_heads, &t)) return TV_ERR_OVERFLOW;
+  int64_t o_bytes, ml_bytes;
+  if (!mul_ok(t, (int64_t)d->head_dim * 4, &o_bytes) || !mul_ok(t, 8, &ml_bytes)) return TV_ERR_OVERFLOW;
+  p->o_part_bytes = align_up(o_bytes, 256);
+  p->ml_part_bytes = align_up(ml_bytes, 256);
+  return TV_OK;
+}
+
+void accept_chunks(int R, int V, int* vchunks, int* vchunk_len) {
+  int sms = num_sms();
+  int want = (2 * sms + R - 1) / R;
+  int maxc = (V + 4095) / 4096;
+  if (want > maxc) want = maxc;
+  if (want < 1) want = 1;
+  int len = (V + want - 1) / want;
+  len = (len + 7) / 8 * 8;
+  *vchunk_len = len;
+  *vchunks = (V + len - 1) / len;
+}
+
+int64_t accept_bytes(const tv_desc* d, int V) {
+  if (V <= 0) return 0;
+  int vc, vl;
+  accept_chunks(d->total_rows, V, &vc, &vl);
+  return 2 * align_up((int64_t)d->total_rows * vc * 4, 256);
+}
+
+cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+int check_attn_ptrs(const tv_desc* d, const void* q, const void* kc, const void* vc, const int32_t* pt,
+                    const int32_t* pl, const int32_t* no, const void* kt, const void* vt, const uint64_t* anc,
+                    const void* ws, int32_t* st) {
+  if (!q || !kc || !vc || !pl || !no || !kt || !vt || !anc || !ws || !st) return TV_ERR_NULL;
+  if (d->page_size == kPageSize && !pt) return TV_ERR_NULL;
+  const void* all[] = {q, kc, vc, pl, no, kt, vt, anc, ws, st};
+  for (const void* p : all)
+    if (!aligned16(p)) return TV_ERR_ALIGN;
+  if (pt && !aligned16(pt)) return TV_ERR_ALIGN;
+  return TV_OK;
+}
+
+AttnParams attn_params(const tv_desc* d, const Plan& pl, const void* q, const void* kc, const void* vc,
+                       const int32_t* pt, const int32_t* plen, const int32_t* no, const void* kt,
+                       const void* vt, const uint64_t* anc, void* ws, int32_t* st) {
+  AttnParams a;
+  a.q = q; a.k_cache = kc; a.v_cache = vc;
+  a.page_table = d->page_size ? pt : nullptr;
+  a.prefix_len = plen; a.node_offsets = no; a.k_tree = kt; a.v_tree = vt; a.anc = anc;
+  a.o_part = reinterpret_cast<float*>(ws);
+  a.ml_part = reinterpret_cast<float2*>(reinterpret_cast<char*>(ws) + pl.o_part_bytes);
+  a.status = st;
+  a.B = d->batch; a.Hq = d->num_q_heads; a.Hkv = d->num_kv_heads; a.G = pl.G; a.d = d->head_dim;
+  a.R = d->total_rows; a.max_nodes = d->max_nodes;
+  a.paged = d->page_size != 0;
+  a.capacity = d->capacity; a.num_pages = d->num_pages;
+  a.max_pages = d->capacity / kPageSize;
+  a.max_prefix = d->max_prefix;
+  float scale = d->scale > 0.f ? d->scale : 1.0f / std::sqrt((float)d->head_dim);
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.chunk = pl.pub.chunk; a.splits = pl.pub.num_splits;
+  a.rows_per_tile = pl.pub.rows_per_tile; a.row_tiles = pl.pub.row_tiles;
+  return a;
+}
+
+int launch_partials(const tv_desc* d, const Plan& pl, const AttnParams& a, cudaStream_t s) {
+  cudaError_t e = pl.pub.kernel == 1 ? launch_attn_tc(a, s) : launch_attn_simt(a, d->dtype, s);
+  return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+}
+
+int launch_merge_from(const tv_desc* d, const Plan& pl, const int32_t* plen, const int32_t* no, void* out,
+                      const void* ws, int32_t* st, cudaStream_t s) {
+  MergeParams m;
+  m.prefix_len = plen; m.node_offsets = no;
+  m.o_part = reinterpret_cast<const float*>(ws);
+  m.ml_part = reinterpret_cast<const float2*>(reinterpret_cast<const char*>(ws) + pl.o_part_bytes);
+  m.out = out; m.status = st;
+  m.B = d->batch; m.Hq = d->num_q_heads; m.d = d->head_dim; m.R = d->total_rows; m.max_nodes = d->max_nodes;
+  m.out_bf16 = (d->dtype == TV_BF16 && !d->out_f32) ? 1 : 0;
+  m.max_prefix = d->max_prefix; m.capacity = d->capacity;
+  m.chunk = pl.pub.chunk; m.splits = pl.pub.num_splits;
+  return launch_merge(m, s) == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace tv
+
+using namespace tv;
+
+extern "C" {
+
+const char* tv_version(void) { return "treeverify 0.1 sm_103a"; }
+
+const char* tv_status_string(int code) {
+  switch (code) {
+    case TV_OK: return "ok";
+    case TV_ERR_NULL: return "null pointer";
+    case TV_ERR_DTYPE: return "unsupported dtype";
+    case TV_ERR_HEAD_DIM: return "unsupported head_dim (128, 256, 512)";
+    case TV_ERR_ZERO_HEADS: return "zero query or KV heads";
+    case TV_ERR_GQA: return "num_q_heads not a multiple of num_kv_heads";
+    case TV_ERR_SHAPE: return "shape out of range";
+    case TV_ERR_TREE: return "tree size out of range (max_nodes 1..64, total_rows)";
+    case TV_ERR_PAGED: return "bad paged-cache description";
+    case TV_ERR_OVERFLOW: return "size overflows int64";
+    case TV_ERR_WORKSPACE: return "workspace too small";
+    case TV_ERR_ALIGN: return "device pointer not 16-byte aligned";
+    case TV_ERR_CUDA: return "CUDA launch failed";
+    case TV_DEV_BAD_TREE: return "device: bad parent pointer";
+    case TV_DEV_BAD_OFFSETS: return "device: bad node offsets";
+    case TV_DEV_BAD_PREFIX: return "device: prefix length out of range";
+    case TV_DEV_BAD_PAGE: return "device: page id out of range";
+    case TV_DEV_CAPACITY: return "device: accepted rows do not fit the cache";
+    case TV_DEV_TIMEOUT: return "device: bounded wait ran out";
+    default: return "unknown";
+  }
+}
+
+int tv_attn_plan(const tv_desc* desc, tv_plan* plan) {
+  int rc = validate(desc);
+  if (rc) return rc;
+  if (!plan) return TV_ERR_NULL;
+  Plan p;
+  rc = make_plan(desc, &p);
+  if (rc) return rc;
+  *plan = p.pub;
+  return TV_OK;
+}
+
+int tv_workspace_size(const tv_desc* desc, int32_t vocab, size_t* bytes) {
+  int rc = validate(desc);
+  if (rc) return rc;
+  if (!bytes) return TV_ERR_NULL;
+  if (vocab < 0) return TV_ERR_SHAPE;
+  Plan p;
+  rc = make_plan(desc, &p);
+  if (rc) return rc;
+  int64_t total = 0;
+  if (!add_ok(p.o_part_bytes, p.ml_part_bytes, &total) || !add_ok(total, accept_bytes(desc, vocab), &total))
+    return TV_ERR_OVERFLOW;
+  *bytes = (size_t)total;
+  return TV_OK;
+}
+
+int tv_build_tree_mask(const tv_desc* desc, const int32_t* d_parents, const int32_t* d_node_offsets,
+                       uint64_t* d_anc, int32_t* d_depth, int32_t* d_status, void* stream) {
+  int rc = validate(desc);
+  if (rc) return rc;
+  if (!d_parents || !d_node_offsets || !d_anc || !d_status) return TV_ERR_NULL;
+  if (!aligned16(d_parents) || !aligned16(d_node_offsets) || !aligned16(d_anc) || !aligned16(d_status) ||
+      (d_depth && !aligned16(d_depth)))
+    return TV_ERR_ALIGN;
+  cudaError_t e = launch_tree_mask(d_parents, d_node_offsets, d_anc, d_depth, d_status, desc->batch,
+                                   desc->total_rows, desc->max_nodes, as_stream(stream));
+  return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+}
+
+int tv_attn_partials(const tv_desc* desc, const void* d_q, const void* d_k_cache, const void* d_v_cache,
+                     const int32_t* d_page_table, const int32_t* d_prefix_len, const int32_t* d_node_offsets,
+                     const void* d_k_tree, const void* d_v_tree, const uint64_t* d_anc, void* d_workspace,
+                     size_t workspace_bytes, int32_t* d_status, void* stream) {
+  int rc = validate(desc);
+  if (rc) return rc;
+  rc = check_attn_ptrs(desc, d_q, d_k_cache, d_v_cache, d_page_table, d_prefix_len, d_node_offsets, d_k_tree,
+                       d_v_tree, d_anc, d_workspace, d_status);
+  if (rc) return rc;
+  Plan p;
+  rc = make_plan(desc, &p);
+  if (rc) return rc;
+  if ((int64_t)workspace_bytes < p.o_part_bytes + p.ml_part_bytes) return TV_ERR_WORKSPACE;
+  AttnParams a = attn_params(desc, p, d_q, d_k_cache, d_v_cache, d_page_table, d_prefix_len, d_node_offsets,
+                             d_k_tree, d_v_tree, d_anc, d_workspace, d_status);
+  return launch_partials(desc, p, a, as_stream(stream));
+}
+
+int tv_attn_merge(const tv_desc* desc, const int32_t* d_prefix_len, const int32_t* d_node_offsets, void* d_out,
+                  const void* d_workspace, size_t workspace_bytes, int32_t* d_status, void* stream) {
+  int rc = validate(desc);
+  if (rc) return rc;
+  if (!d_prefix_len || !d_node_offsets || !d_out || !d_workspace || !d_status) return TV_ERR_NULL;
+  if (!aligned16(d_prefix_len) || !aligned16(d_node_offsets) || !aligned16(d_out) || !aligned16(d_workspace) ||
+      !aligned16(d_status))
+    return TV_ERR_ALIGN;
+  Plan p;
+  rc = make_plan(desc, &p);
+  if (rc) return rc;
+  if ((int64_t)workspace_bytes < p.o_part_bytes + p.ml_part_bytes) return TV_ERR_WORKSPACE;
+  return launch_merge_from(desc, p, d_prefix_len, d_node_offsets, d_out, d_workspace, d_status,
+                           as_stream(stream));
+}
+
+int tree_verify_attn(const tv_desc* desc, const void* d_q, const void* d_k_cache, const void* d_v_cache,
+                     const int32_t* d_page_table, const int32_t* d_prefix_len, const int32_t* d_node_offsets,
+                     const void* d_k_tree, const void* d_v_tree, const uint64_t* d_anc, void* d_out,
+                     void* d_workspace, size_t workspace_bytes, int32_t* d_status, void* stream) {
+  int rc = validate(desc);
+  if (rc) return rc;
+  rc = check_attn_ptrs(desc, d_q, d_k_cache, d_v_cache, d_page_table, d_prefix_len, d_node_offsets, d_k_tree,
+                       d_v_tree, d_anc, d_workspace, d_status);
+  if (rc) return rc;
+  if (!d_out) return TV_ERR_NULL;
+  if (!aligned16(d_out)) return TV_ERR_ALIGN;
+  Plan p;
+  rc = make_plan(desc, &p);
+  if (rc) return rc;
+  if ((int64_t)workspace_bytes < p.o_part_bytes + p.ml_part_bytes) return TV_ERR_WORKSPACE;
+  AttnParams a = attn_params(desc, p, d_q, d_k_cache, d_v_cache, d_page_table, d_prefix_len, d_node_offsets,
+                             d_k_tree, d_v_tree, d_anc, d_workspace, d_status);
+  cudaStream_t s = as_stream(stream);
+  rc = launch_partials(desc, p, a, s);
+  if (rc) return rc;
+  return launch_merge_from(desc, p, d_prefix_len, d_node_offsets, d_out, d_workspace, d_status, s);
+}
+
+int tree_accept_commit(const tv_desc* desc, int32_t vocab, int32_t logits_dtype, const void* d_logits,
+                       const int32_t* d_draft_tokens, const int32_t* d_parents, const int32_t* d_node_offsets,
+                       const void* d_k_tree, const void* d_v_tree, void* d_k_cache, void* d_v_cache,
+                       const int32_t* d_page_table, int32_t* d_prefix_len, int32_t* d_argmax,
+                       int32_t* d_accept_len, int32_t* d_path, int32_t* d_tokens, void* d_workspace,
+                       size_t workspace_bytes, int32_t* d_status, void* stream) {
+  int rc = validate(desc);
+  if (rc) return rc;
+  if (logits_dtype != TV_F32 && logits_dtype != TV_BF16) return TV_ERR_DTYPE;
+  if (vocab < 1) return TV_ERR_SHAPE;
+  if (!d_logits || !d_draft_tokens || !d_parents || !d_node_offsets || !d_k_tree || !d_v_tree || !d_k_cache ||
+      !d_v_cache || !d_prefix_len || !d_argmax || !d_accept_len || !d_path || !d_tokens || !d_workspace ||
+      !d_status)
+    return TV_ERR_NULL;
+  if (desc->page_size == kPageSize && !d_page_table) return TV_ERR_NULL;
+  const void* all[] = {d_logits, d_draft_tokens, d_parents, d_node_offsets, d_k_tree, d_v_tree, d_k_cache,
+                       d_v_cache, d_prefix_len, d_argmax, d_accept_len, d_path, d_tokens, d_workspace, d_status};
+  for (const void* ptr : all)
+    if (!aligned16(ptr)) return TV_ERR_ALIGN;
+  if (d_page_table && !aligned16(d_page_table)) return TV_ERR_ALIGN;
+  int64_t lb;
+  if (!mul_ok(desc->total_rows, vocab, &lb) || !mul_ok(lb, 4, &lb)) return TV_ERR_OVERFLOW;
+  Plan p;
+  rc = make_plan(desc, &p);
+  if (rc) return rc;
+  int64_t off = p.o_part_bytes + p.ml_part_bytes;
+  if ((int64_t)workspace_bytes < off + accept_bytes(desc, vocab)) return TV_ERR_WORKSPACE;
+  AcceptParams a;
+  a.logits = d_logits; a.logits_bf16 = logits_dtype == TV_BF16; a.V = vocab;
+  a.draft = d_draft_tokens; a.parents = d_parents; a.node_offsets = d_node_offsets;
+  a.k_tree = d_k_tree; a.v_tree = d_v_tree; a.k_cache = d_k_cache; a.v_cache = d_v_cache;
+  a.page_table = desc->page_size ? d_page_table : nullptr;
+  a.prefix_len = d_prefix_len; a.argmax = d_argmax; a.accept_len = d_accept_len;
+  a.path = d_path; a.tokens = d_tokens; a.status = d_status;
+  accept_chunks(desc->total_rows, vocab, &a.vchunks, &a.vchunk_len);
+  int64_t part = align_up((int64_t)desc->total_rows * a.vchunks * 4, 256);
+  a.am_val = reinterpret_cast<float*>(reinterpret_cast<char*>(d_workspace) + off);
+  a.am_idx = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(d_workspace) + off + part);
+  a.B = desc->batch; a.R = desc->total_rows; a.Hkv = desc->num_kv_heads; a.d = desc->head_dim;
+  a.esize = desc->dtype == TV_BF16 ? 2 : 4; a.max_nodes = desc->max_nodes; a.paged = desc->page_size != 0;
+  a.capacity = desc->capacity; a.num_pages = desc->num_pages; a.max_pages = desc->capacity / kPageSize;
+  cudaError_t e = launch_accept_commit(a, as_stream(stream));
+  return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+}
+
+}  // extern "C"

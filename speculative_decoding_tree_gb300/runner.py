@@ -1,0 +1,87 @@
+"""Device-resident buffers for one verify workload and the C-ABI calls of a
+verify step, in stream order: tree mask, attention, accept + commit.
+
+Used by the benchmark, the GPU tests and the smoke check.  It only moves a
+workload's tensors to the GPU, allocates the outputs and workspace with
+torch, and calls the library; it computes nothing itself.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (BF16, F32, make_desc, tree_accept_commit, tree_verify_attn, tv_attn_merge, tv_attn_partials,
+               tv_build_tree_mask, tv_workspace_size)
+
+_DT = {torch.float32: F32, torch.bfloat16: BF16}
+
+
+class DeviceStep:
+    def __init__(self, w, device="cuda", out_f32=False, max_prefix=None, vocab=None, max_nodes=None):
+        self.w = w
+        dev = torch.device(device)
+        self.device = dev
+        sp = w.spec
+        self.dtype = _DT[w.q.dtype]
+        self.logits_dtype = _DT[w.logits.dtype]
+        self.vocab = vocab if vocab is not None else w.logits.shape[1]
+        mp = int(w.prefix_len.max()) if max_prefix is None else int(max_prefix)
+        self.desc = make_desc(
+            batch=sp.batch, num_q_heads=sp.hq, num_kv_heads=sp.hkv, head_dim=sp.d, dtype=self.dtype,
+            max_nodes=w.max_nodes if max_nodes is None else int(max_nodes), total_rows=w.total_rows, capacity=w.capacity, max_prefix=mp,
+            page_size=16 if w.page_table is not None else 0,
+            num_pages=w.k_cache.shape[0] if w.page_table is not None else 0,
+            out_f32=int(out_f32))
+        to = lambda t: None if t is None else t.to(dev).contiguous()
+        self.q, self.k_tree, self.v_tree = to(w.q), to(w.k_tree), to(w.v_tree)
+        self.k_cache, self.v_cache = to(w.k_cache), to(w.v_cache)
+        self.page_table = to(w.page_table)
+        self.prefix_len = to(w.prefix_len)
+        self.node_offsets = to(w.node_offsets)
+        self.parents = to(w.parents_flat)
+        self.logits = to(w.logits)
+        self.draft = to(w.draft_tokens) if w.draft_tokens is not None else None
+        R, B, mn = w.total_rows, sp.batch, self.desc.max_nodes
+        self.anc = torch.zeros(R, dtype=torch.int64, device=dev)
+        self.depth = torch.zeros(R, dtype=torch.int32, device=dev)
+        odt = torch.float32 if (self.dtype == F32 or out_f32) else torch.bfloat16
+        self.out = torch.zeros(R, sp.hq, sp.d, dtype=odt, device=dev)
+        self.status = torch.zeros(4, dtype=torch.int32, device=dev)
+        self.argmax = torch.zeros(R, dtype=torch.int32, device=dev)
+        self.accept_len = torch.zeros(B, dtype=torch.int32, device=dev)
+        self.path = torch.zeros(B, mn, dtype=torch.int32, device=dev)
+        self.tokens = torch.zeros(B, mn, dtype=torch.int32, device=dev)
+        self.ws_bytes = tv_workspace_size(self.desc, self.vocab)
+        self.workspace = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
+
+    # one call each ------------------------------------------------------
+    def mask(self, stream=None):
+        tv_build_tree_mask(self.desc, self.parents, self.node_offsets, self.anc, self.depth, self.status, stream)
+
+    def attn(self, stream=None):
+        tree_verify_attn(self.desc, self.q, self.k_cache, self.v_cache, self.page_table, self.prefix_len,
+                         self.node_offsets, self.k_tree, self.v_tree, self.anc, self.out, self.workspace,
+                         self.ws_bytes, self.status, stream)
+
+    def partials(self, stream=None):
+        tv_attn_partials(self.desc, self.q, self.k_cache, self.v_cache, self.page_table, self.prefix_len,
+                         self.node_offsets, self.k_tree, self.v_tree, self.anc, self.workspace, self.ws_bytes,
+                         self.status, stream)
+
+    def merge(self, stream=None):
+        tv_attn_merge(self.desc, self.prefix_len, self.node_offsets, self.out, self.workspace, self.ws_bytes,
+                      self.status, stream)
+
+    def accept_commit(self, stream=None):
+        tree_accept_commit(self.desc, self.vocab, self.logits_dtype, self.logits, self.draft, self.parents,
+                           self.node_offsets, self.k_tree, self.v_tree, self.k_cache, self.v_cache,
+                           self.page_table, self.prefix_len, self.argmax, self.accept_len, self.path,
+                           self.tokens, self.workspace, self.ws_bytes, self.status, stream)
+
+    def step(self, stream=None):
+        """One verify step: mask, attention, accept + commit."""
+        self.mask(stream)
+        self.attn(stream)
+        self.accept_commit(stream)
+
+    # launches of our kernels in one step (mask 1, split 1, merge 1, argmax 1, walk+commit 1)
+    KERNELS_PER_STEP = 5

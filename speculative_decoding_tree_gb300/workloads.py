@@ -265,7 +265,7 @@ def make_workload(spec: Spec, canary: float = float("nan"),
 
     # 6. coins and replacement tokens
     coins = torch.rand(total, generator=gen, dtype=torch.float64)
-    repl = torch.randint(0, spec.vocab - 1, (total,), generator=gen)
+    repl = torch.randint(0, max(spec.vocab - 1, 1), (total,), generator=gen)
     repl_full = torch.randint(0, spec.vocab, (total,), generator=gen)
 
     # cache layout
@@ -330,7 +330,7 @@ def plant_drafts(w: Workload, am) -> torch.Tensor:
         for i in range(1, len(ps)):
             r = o + i
             target = int(am[o + ps[i]])
-            miss = int(w.repl[r]) + (1 if int(w.repl[r]) >= target else 0)
+            miss = min(int(w.repl[r]) + (1 if int(w.repl[r]) >= target else 0), V - 1)
             if w.spec.tree == "config1":
                 mode = planted[i]
             else:

@@ -1,0 +1,101 @@
+"""The C-ABI library loads, exports every symbol include/tree_verify.h
+declares, and rejects bad arguments on the host before any launch.  CPU only:
+no call here reaches a kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import speculative_decoding_tree_gb300 as tv
+from speculative_decoding_tree_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tree_verify.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return tv.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?(?:int|size_t|char\s*\*|void)\s*\**\s*(\w+)\s*\(", text,
+                                 flags=re.M)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert {"tree_verify_attn", "tree_accept_commit", "tv_build_tree_mask", "tv_workspace_size"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_codes_have_names(L):
+    for code in range(0, -13, -1):
+        assert tv.tv_status_string(code) != "unknown"
+    for bit in (1, 2, 4, 8, 16, 32):
+        assert tv.tv_status_string(bit).startswith("device:")
+    assert tv.tv_status_string(12345) == "unknown"
+    assert "sm_103a" in tv.tv_version()
+
+
+def _desc(**kw):
+    base = dict(batch=1, num_q_heads=32, num_kv_heads=8, head_dim=256, dtype=tv.BF16, max_nodes=64,
+                total_rows=64, capacity=4176, max_prefix=4096)
+    base.update(kw)
+    return tv.make_desc(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(num_kv_heads=0), -4), (dict(num_q_heads=0), -4), (dict(num_q_heads=30), -5),
+    (dict(head_dim=64), -3), (dict(dtype=7), -2), (dict(max_nodes=65, total_rows=65), -7),
+    (dict(total_rows=65), -7), (dict(batch=0), -6), (dict(max_prefix=5000), -6),
+    (dict(page_size=8), -8), (dict(page_size=16, num_pages=0), -8), (dict(page_size=16, capacity=4177), -8),
+    (dict(capacity=2 ** 62, max_prefix=4096), -9), (dict(scale=float("nan")), -6),
+])
+def test_descriptor_validation(L, kw, code):
+    d = _desc(**kw)
+    n = ctypes.c_size_t(0)
+    assert L.tv_workspace_size(ctypes.byref(d), 1000, ctypes.byref(n)) == code
+    # the same code from the launch entry points, which return before launching
+    fake = 1 << 20
+    rc = L.tree_verify_attn(ctypes.byref(d), *([fake] * 10), fake, 1 << 30, fake, None)
+    assert rc == code
+
+
+def test_null_and_alignment_and_workspace(L):
+    d = _desc()
+    fake = 1 << 20
+    ptrs = [fake] * 10
+    assert L.tree_verify_attn(None, *ptrs, fake, 1 << 30, fake, None) == -1
+    bad = list(ptrs)
+    bad[0] = None
+    assert L.tree_verify_attn(ctypes.byref(d), *bad, fake, 1 << 30, fake, None) == -1
+    bad[0] = fake + 8
+    assert L.tree_verify_attn(ctypes.byref(d), *bad, fake, 1 << 30, fake, None) == -11
+    assert L.tree_verify_attn(ctypes.byref(d), *ptrs, fake, 16, fake, None) == -10
+    # paged cache requires a page table
+    dp = _desc(page_size=16, num_pages=300, capacity=4176)
+    bad = list(ptrs)
+    bad[3] = None
+    assert L.tree_verify_attn(ctypes.byref(dp), *bad, fake, 1 << 30, fake, None) == -1
+    # accept: bad logits dtype, vocab, workspace
+    args = [fake] * 15
+    assert L.tree_accept_commit(ctypes.byref(d), 1000, 5, *args, 1 << 30, fake, None) == -2
+    assert L.tree_accept_commit(ctypes.byref(d), 0, 1, *args, 1 << 30, fake, None) == -6
+    assert L.tree_accept_commit(ctypes.byref(d), 1000, 1, *args, 64, fake, None) == -10
+
+
+def test_workspace_and_plan(L):
+    d = _desc()
+    ws = tv.tv_workspace_size(d, 151936)
+    assert ws > tv.tv_workspace_size(d, 0) > 0
+    plan = tv.tv_attn_plan(d)
+    assert plan["num_splits"] >= 1 and plan["chunk"] * plan["num_splits"] >= 4096
+    assert plan["rows_per_tile"] * plan["row_tiles"] >= 64 * 4
+    f32 = tv.tv_attn_plan(_desc(dtype=tv.F32))
+    assert f32["kernel"] == 0
