@@ -235,6 +235,37 @@ int tree_accept_commit(const tv_desc* desc, int32_t vocab, int32_t logits_dtype,
                        int32_t* d_path, int32_t* d_tokens, void* d_workspace, size_t workspace_bytes,
                        int32_t* d_status, void* stream);
 
+/* ------------------------------------- attention without a workspace */
+
+/* Size in bytes of the library's static scratch array (file-scope device
+ * memory) that tree_verify_attn_noalloc uses instead of a caller workspace. */
+#define TV_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* tree_verify_attn for callers that cannot allocate device memory: a
+ * plugin that a host framework hands only its input and output buffers, or
+ * a loop that must not call cudaMalloc (it may synchronise the device).
+ * The pages have no counterpart of this call; it exists for such callers.
+ * Same arguments and results as tree_verify_attn minus the workspace: the
+ * split-KV partials go to a static __device__ array of
+ * TV_NOALLOC_SCRATCH_BYTES (32 MiB), which every GPU that loads this part of
+ * the library keeps until the process exits.
+ * - Returns TV_ERR_WORKSPACE, enqueuing nothing, when the descriptor needs
+ *   more partials than the array holds (tv_workspace_size(desc, 0) above
+ *   TV_NOALLOC_SCRATCH_BYTES).
+ * - The first call on a device looks up the array's device address with
+ *   that device current (the caller's current device; `stream` must belong
+ *   to it) and keeps it; make that first call before any stream capture.
+ *   TV_ERR_CUDA if the lookup fails.
+ * - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ * - Every call shares the one array and it keeps the last call's contents;
+ *   nothing in it needs to start at zero (each call writes every partial it
+ *   reads).  Calls whose kernels overlap on the GPU (other streams, other
+ *   host threads) race on the array: serialise them. */
+int tree_verify_attn_noalloc(const tv_desc* desc, const void* d_q, const void* d_k_cache, const void* d_v_cache,
+                             const int32_t* d_page_table, const int32_t* d_prefix_len,
+                             const int32_t* d_node_offsets, const void* d_k_tree, const void* d_v_tree,
+                             const uint64_t* d_anc, void* d_out, int32_t* d_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
