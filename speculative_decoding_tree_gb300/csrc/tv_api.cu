@@ -70,7 +70,7 @@ struct Plan {
 
 int make_plan(const tv_desc* d, Plan* p) {
   int G = d->num_q_heads / d->num_kv_heads;
-  bool tc = d->dtype == TV_BF16 && d->max_nodes * G >= 16 && tc_supported(d->head_dim, G, d->dtype, d->max_nodes);
+  bool tc = d->dtype == TV_BF16 && d->max_nodes * G >= 16 && tc_supported(d, G);
   int key_tile = tc ? tc_key_tile(d->head_dim) : 32;
   int rows_per_tile;
   if (tc) {

@@ -1,11 +1,502 @@
-// tcgen05 tensor-core split-KV tree-verify attention (placeholder until the
-// kernel lands: no descriptor selects it).
+// tcgen05 tensor-core split-KV tree-verify attention (bf16 Q/K/V, fp32
+// accumulation and softmax), head_dim 128 or 256.
+//
+// The method is flash-decode with a tree mask ("ADR-037 — EAGLE-3 with
+// dynamic tree port", phase rows E1.1-E1.5 and E4b.6): each CTA walks a
+// chunk of keys with an online softmax and leaves an unnormalised partial
+// output O, its running maximum m (base-2 units: score * scale * log2 e) and
+// running sum l; merge_kernel combines the chunks.
+//
+// CTA = (128-row query tile, KV head g, key chunk s, sequence b).  Query row
+// m of a tile is node m / G, group head m % G of KV head g, so the G query
+// heads that share a KV head form one dense M=128 tile and every K/V tile is
+// read once for all of them.
+//
+//   warp 0      TMA producer: the Q tile once, then 32 KB K/V chunks (128 keys
+//               x 128 columns, 128-byte swizzled) through a ring of slots in
+//               exactly the order the MMA consumes them: K(0), K(1), V(0),
+//               K(2), V(1), ...
+//   warp 1      owns tensor memory; lane 0 issues tcgen05.mma:
+//               S(t) = Q K(t)^T into one of two 128-column TMEM buffers, then
+//               O += P(t-1) V(t-1) with P read from TMEM.
+//   warps 4-7   softmax, one thread per query row (its TMEM lane): load the
+//               S row, mask, running max, P = 2^(s*c - m) written back over
+//               the S columns as bf16 pairs, running sum; rescale the O row
+//               in TMEM only when the maximum grows by more than 2^8; at the
+//               end write the partial (O, m, l).
+//
+// Keys: the chunk's prefix positions in 128-key tiles, then (in the last
+// chunk of the sequence) one tile of the sequence's tree keys masked by the
+// row's ancestor bits.  Rows past the prefix end in the last tile are masked
+// in S and zeroed in the V chunk (0 x NaN would poison P V).
+//
+// Every mbarrier wait is bounded (1 s); on a timeout the CTA raises
+// TV_DEV_TIMEOUT, drains its own copies and MMAs, frees tensor memory and
+// returns.
+#include <cuda.h>
+
+#include <mutex>
+
+#include "tc_ptx.cuh"
 #include "tv_internal.cuh"
 
 namespace tv {
+namespace {
 
-bool tc_supported(int, int, int, int) { return false; }
-int tc_key_tile(int) { return 64; }
-cudaError_t launch_attn_tc(const AttnParams&, cudaStream_t) { return cudaErrorNotSupported; }
+using namespace tc;
+
+constexpr int BM = 128;                         // query rows per tile
+constexpr int BN = 128;                         // keys per tile
+constexpr int CH = 128;                         // columns of d per chunk
+constexpr uint32_t BOX_BYTES = BN * 128;        // one TMA box: 128 rows x 64 bf16
+constexpr uint32_t CHUNK_BYTES = 2 * BOX_BYTES; // 128 keys x 128 columns
+constexpr uint64_t kWaitNs = 1000000000ull;
+constexpr float kRescaleThreshold = 8.0f;       // rescale O when the max grows by > 2^8
+
+template <int D>
+struct Cfg {
+  static constexpr int CPT = D / CH;              // chunks per K (or V) tile
+  static constexpr int NS = D == 256 ? 5 : 6;     // ring slots
+  static constexpr uint32_t Q_BYTES = BM * D * 2;
+  static constexpr uint32_t RING_BYTES = NS * CHUNK_BYTES;
+  static constexpr int NBARS = 2 * NS + 9;
+  static constexpr uint32_t SMEM = 1024 + Q_BYTES + RING_BYTES + NBARS * 8 + 16;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <int D>
+__global__ void __launch_bounds__(256, 1)
+tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tm_q,
+                  const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_vc,
+                  const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_vt) {
+  using C = Cfg<D>;
+  constexpr int CPT = C::CPT, NS = C::NS;
+  extern __shared__ uint8_t smem_raw[];
+
+  // ---------------------------------------------------------------- work
+  const int rt = blockIdx.x;
+  const int g = blockIdx.y / p.splits;
+  const int s = blockIdx.y % p.splits;
+  const int b = blockIdx.z;
+  int o0, n;
+  if (!seq_rows(p.node_offsets, b, p.R, p.max_nodes, p.status, &o0, &n)) return;
+  const int G = p.G;
+  const int nrows = n * G;
+  const int m0 = rt * p.rows_per_tile;
+  if (m0 >= nrows) return;
+  const int64_t Praw = p.prefix_len[b];
+  const int64_t P = clamp_prefix(Praw, p.max_prefix, p.capacity);
+  if (P != Praw && threadIdx.x == 0 && rt == 0 && s == 0 && g == 0) set_status(p.status, TV_DEV_BAD_PREFIX);
+  const int nch = num_chunks(P, p.chunk);
+  if (s >= nch) return;
+  const int64_t k_begin = (int64_t)s * p.chunk;
+  const int64_t k_end = min(P, k_begin + p.chunk);
+  const bool has_tree = (s == nch - 1);
+  const int npt = (int)((k_end - k_begin + BN - 1) / BN);      // prefix tiles
+  const int T = npt + (has_tree ? 1 : 0);
+  const int tail_valid = npt > 0 ? (int)(k_end - (k_begin + (int64_t)(npt - 1) * BN)) : BN;
+
+  // ---------------------------------------------------------------- smem
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = base;
+  uint8_t* ring = base + C::Q_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ring + C::RING_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  auto FULL = [&](int i) { return bar(i); };
+  auto EMPTY = [&](int i) { return bar(NS + i); };
+  const uint32_t Q_FULL = bar(2 * NS), S_FULL0 = bar(2 * NS + 1), P_FULL0 = bar(2 * NS + 3);
+  const uint32_t O_DONE0 = bar(2 * NS + 5), TAIL = bar(2 * NS + 7), FIN = bar(2 * NS + 8);
+  auto S_FULL = [&](int i) { return S_FULL0 + 8 * i; };   // QK(t) done, buffer t & 1
+  auto P_FULL = [&](int i) { return P_FULL0 + 8 * i; };   // softmax wrote P(t), buffer t & 1
+  auto O_DONE = [&](int i) { return O_DONE0 + 8 * i; };   // PV(t) done, alternating by t & 1
+  constexpr unsigned kAll = 0xffffffffu;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(FULL(i), 1);
+      mbar_init(EMPTY(i), 1);
+    }
+    mbar_init(Q_FULL, 1);
+    mbar_init(S_FULL(0), 1);
+    mbar_init(S_FULL(1), 1);
+    mbar_init(P_FULL(0), 128);
+    mbar_init(P_FULL(1), 128);
+    mbar_init(O_DONE(0), 1);
+    mbar_init(O_DONE(1), 1);
+    mbar_init(TAIL, 1);
+    mbar_init(FIN, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (p.rows_per_tile < BM) {
+    // pad rows of the query tile (G does not divide 128) hold zeros
+    const int pad = BM - p.rows_per_tile;
+    for (int e = tid; e < (D / 64) * pad * 8; e += blockDim.x) {
+      const int kb = e / (pad * 8), r = p.rows_per_tile + (e / 8) % pad, c = e % 8;
+      *reinterpret_cast<uint4*>(sQ + kb * (BM * 128) + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ============================================================ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_kc);
+      tma_prefetch_desc(&tm_vc);
+      mbar_expect_tx(Q_FULL, (uint32_t)p.rows_per_tile * 128u * (D / 64));
+      for (int kb = 0; kb < D / 64; ++kb)
+        tma_load_3d(smem_u32(sQ + kb * (BM * 128)), &tm_q, Q_FULL, kb * 64, g * G, o0 + m0 / G);
+    }
+    int j = 0, tail_uses = 0;
+    bool ok = true;
+    for (int t = 0; t <= T && ok; ++t) {
+      for (int kind = 0; kind < 2 && ok; ++kind) {           // 0: K(t), 1: V(t-1)
+        const int tile = kind == 0 ? t : t - 1;
+        if ((kind == 0 && t >= T) || (kind == 1 && t < 1)) continue;
+        const bool tree = (tile == npt);
+        const bool tail_fix = (kind == 1) && !tree && tile == npt - 1 && tail_valid < BN;
+        for (int c = 0; c < CPT && ok; ++c, ++j) {
+          const int slot = j % NS, use = j / NS;
+          if (use > 0 && !__all_sync(kAll, mbar_wait(EMPTY(slot), (use - 1) & 1, abort_flag, kWaitNs))) {
+            ok = false;
+            break;
+          }
+          uint8_t* dst = ring + slot * CHUNK_BYTES;
+          const uint32_t fb = tail_fix ? TAIL : FULL(slot);
+          if (lane == 0) {
+            if (tree) {
+              mbar_expect_tx(fb, CHUNK_BYTES);
+              const CUtensorMap* m = kind == 0 ? &tm_kt : &tm_vt;
+              for (int bx = 0; bx < 2; ++bx)
+                tma_load_2d(smem_u32(dst + bx * BOX_BYTES), m, fb, c * CH + bx * 64, g * p.R + o0);
+            } else if (!p.paged) {
+              mbar_expect_tx(fb, CHUNK_BYTES);
+              const CUtensorMap* m = kind == 0 ? &tm_kc : &tm_vc;
+              const int64_t row = ((int64_t)b * p.Hkv + g) * p.capacity + k_begin + (int64_t)tile * BN;
+              for (int bx = 0; bx < 2; ++bx)
+                tma_load_2d(smem_u32(dst + bx * BOX_BYTES), m, fb, c * CH + bx * 64, (int)row);
+            } else {
+              const CUtensorMap* m = kind == 0 ? &tm_kc : &tm_vc;
+              const int64_t t0 = k_begin + (int64_t)tile * BN;
+              const int valid = (int)min((int64_t)BN, k_end - t0);
+              const int npages = (valid + kPageSize - 1) / kPageSize;
+              mbar_expect_tx(fb, (uint32_t)npages * 2u * (kPageSize * 128u));
+              const int oob_row = (int)(p.num_pages * p.Hkv * kPageSize);
+              for (int pg = 0; pg < npages; ++pg) {
+                const int64_t pos = t0 + pg * kPageSize;
+                const int pid = p.page_table[(int64_t)b * p.max_pages + pos / kPageSize];
+                int row = oob_row;
+                if (pid >= 0 && pid < p.num_pages) {
+                  row = (int)(((int64_t)pid * p.Hkv + g) * kPageSize);
+                } else if (c == 0) {
+                  set_status(p.status, TV_DEV_BAD_PAGE);
+                }
+                for (int bx = 0; bx < 2; ++bx)
+                  tma_load_2d(smem_u32(dst + bx * BOX_BYTES + pg * kPageSize * 128), m, fb, c * CH + bx * 64, row);
+              }
+            }
+          }
+          __syncwarp();
+          if (tail_fix) {
+            // the chunk's rows past the prefix end become zeros before the MMA reads them
+            if (!__all_sync(kAll, mbar_wait(TAIL, tail_uses & 1, abort_flag, kWaitNs))) {
+              ok = false;
+              break;
+            }
+            ++tail_uses;
+            const int nz = BN - tail_valid;
+            for (int e = lane; e < 2 * nz * 8; e += 32) {
+              const int bx = e / (nz * 8), r = tail_valid + (e / 8) % nz, q16 = e % 8;
+              *reinterpret_cast<uint4*>(dst + bx * BOX_BYTES + r * 128 + q16 * 16) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(FULL(slot));
+          }
+        }
+      }
+    }
+    // drain: every copy this warp started has landed before the CTA exits
+    if (lane == 0) {
+      mbar_wait(Q_FULL, 0, abort_flag, kWaitNs);
+      for (int jj = (j > NS ? j - NS : 0); jj < j; ++jj) mbar_wait(FULL(jj % NS), (jj / NS) & 1, abort_flag, kWaitNs);
+    }
+  } else if (warp == 1) {
+    // ============================================================ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t ID_QK = idesc_bf16_f32(BM, BN, 0, 0);
+      constexpr uint32_t ID_PV = idesc_bf16_f32(BM, CH, 0, 1);
+      bool ok = mbar_wait(Q_FULL, 0, abort_flag, kWaitNs);
+      tc_fence_after();
+      const uint32_t q_addr = smem_u32(sQ);
+      const uint32_t ring_addr = smem_u32(ring);
+      int j = 0;
+      for (int t = 0; t <= T && ok; ++t) {
+        if (t < T) {
+          const uint32_t sbuf = tmem + (uint32_t)((t & 1) * 128);
+          for (int c = 0; c < CPT && ok; ++c, ++j) {
+            const int slot = j % NS;
+            if (!mbar_wait(FULL(slot), (j / NS) & 1, abort_flag, kWaitNs)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t kaddr = ring_addr + slot * CHUNK_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < CH / 16; ++kk) {
+              const int kg = c * (CH / 16) + kk;           // 16-column step over d
+              const uint64_t a = smem_desc(q_addr + (kg >> 2) * (BM * 128) + (kg & 3) * 32, 16, 1024, 2);
+              const uint64_t bd = smem_desc(kaddr + (kk >> 2) * BOX_BYTES + (kk & 3) * 32, 16, 1024, 2);
+              mma_ss(sbuf, a, bd, ID_QK, (c > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(EMPTY(slot));
+          }
+          if (!ok) break;
+          mma_commit(S_FULL(t & 1));
+        }
+        if (t >= 1) {
+          const int u = t - 1;
+          const uint32_t pbuf = tmem + (uint32_t)((u & 1) * 128);
+          if (!mbar_wait(P_FULL(u & 1), (u >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
+          tc_fence_after();
+          for (int c = 0; c < CPT && ok; ++c, ++j) {
+            const int slot = j % NS;
+            if (!mbar_wait(FULL(slot), (j / NS) & 1, abort_flag, kWaitNs)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t vaddr = ring_addr + slot * CHUNK_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk) {       // 16 keys per step
+              const uint64_t bd = smem_desc(vaddr + kk * (16 * 128), BOX_BYTES, 1024, 2);
+              mma_ts(tmem + 256 + c * CH, pbuf + kk * 8, bd, ID_PV, (u > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(EMPTY(slot));
+          }
+          if (!ok) break;
+          mma_commit(O_DONE(u & 1));
+        }
+      }
+      // every MMA this thread issued has finished before tensor memory is freed
+      mma_commit(FIN);
+      mbar_wait(FIN, 0, abort_flag, kWaitNs);
+    }
+  } else if (warp >= 4) {
+    // ============================================================ softmax
+    // Every tcgen05.ld / st below is warp-collective (.sync.aligned): control
+    // flow around them stays warp-uniform, per-row choices only pick values.
+    const int r = tid - 128;                                // row in the tile == TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
+    const bool row_ok = r < p.rows_per_tile && (m0 + r) < nrows;
+    const int node = (m0 + r) / G;
+    const uint64_t anc = row_ok ? p.anc[o0 + node] : 0ull;
+    const float c2 = p.scale_log2;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int t = 0; t < T && ok; ++t) {
+      if (!__all_sync(kAll, mbar_wait(S_FULL(t & 1), (t >> 1) & 1, abort_flag, kWaitNs))) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t sbuf = tmem + lane_base + (uint32_t)((t & 1) * 128);
+      float sv[BN];
+#pragma unroll
+      for (int q = 0; q < BN / 32; ++q) {
+        uint32_t rr[32];
+        tmem_ld_x32(sbuf + q * 32, rr);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) sv[q * 32 + e] = __uint_as_float(rr[e]);
+      }
+      // mask: tree tile -> ancestor bits; partial last prefix tile -> key range
+      const bool tree = (t == npt);
+      const int lim = tree ? min(n, 64) : ((t == npt - 1) ? tail_valid : BN);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < BN; ++e) {
+        bool vis = e < lim;
+        if (tree) vis = vis && ((anc >> (e & 63)) & 1ull);
+        sv[e] = vis ? sv[e] : -INFINITY;
+        mx = fmaxf(mx, sv[e]);
+      }
+      const float m_tile = mx == -INFINITY ? -INFINITY : mx * c2;
+      const float m_new = fmaxf(m_ref, m_tile);
+      const bool first = (m_ref == -INFINITY);              // nothing accumulated yet
+      const bool need = !first && (m_new > m_ref + kRescaleThreshold);
+      if (__any_sync(kAll, need)) {
+        // the O rows must hold P(t-1) V(t-1) before they are rescaled (t >= 1 here)
+        const int u = t - 1;
+        if (!__all_sync(kAll, mbar_wait(O_DONE(u & 1), (u >> 1) & 1, abort_flag, kWaitNs))) { ok = false; break; }
+        tc_fence_after();
+        const float alpha = need ? ex2(m_ref - m_new) : 1.f;
+#pragma unroll 1
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t rr[32];
+          const uint32_t oa = tmem + lane_base + 256 + q * 32;
+          tmem_ld_x32(oa, rr);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
+          tmem_st_x32(oa, rr);
+        }
+        if (need) {
+          l *= alpha;
+          m_ref = m_new;
+        }
+      }
+      if (first) m_ref = m_new;
+      const bool live = m_ref != -INFINITY;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float x0 = sv[h * 64 + 2 * e], x1 = sv[h * 64 + 2 * e + 1];
+          const float p0 = live ? ex2(fmaf(x0, c2, -m_ref)) : 0.f;
+          const float p1 = live ? ex2(fmaf(x1, c2, -m_ref)) : 0.f;
+          l += p0 + p1;
+          pk[e] = pack_bf16(p0, p1);
+        }
+        tmem_st_x32(sbuf + h * 32, pk);
+      }
+      tc_fence_before();
+      mbar_arrive(P_FULL(t & 1));
+    }
+    // epilogue: the last P V has landed (its commit covers every earlier MMA);
+    // write this chunk's partial
+    const int u = T - 1;
+    if (ok && __all_sync(kAll, mbar_wait(O_DONE(u & 1), (u >> 1) & 1, abort_flag, kWaitNs))) {
+      tc_fence_after();
+      const int64_t rowg = o0 + node;
+      const int h = g * G + (m0 + r) % G;
+      const int64_t idx = ((int64_t)s * p.R + rowg) * p.Hq + h;
+      float4* dst = reinterpret_cast<float4*>(p.o_part + idx * D);
+#pragma unroll 1
+      for (int q = 0; q < D / 32; ++q) {
+        uint32_t rr[32];
+        tmem_ld_x32(tmem + lane_base + 256 + q * 32, rr);
+        if (row_ok) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            dst[q * 8 + e] = make_float4(__uint_as_float(rr[4 * e]), __uint_as_float(rr[4 * e + 1]),
+                                         __uint_as_float(rr[4 * e + 2]), __uint_as_float(rr[4 * e + 3]));
+        }
+      }
+      if (row_ok) p.ml_part[idx] = make_float2(m_ref, l);
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0 && *abort_flag) set_status(p.status, TV_DEV_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------- host
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+bool encode(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+            const cuuint32_t* box) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_tc_t(const AttnParams& p, cudaStream_t st) {
+  CUtensorMap mq, mkc, mvc, mkt, mvt;
+  const cuuint64_t row_bytes = (cuuint64_t)D * 2;
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.Hq, (cuuint64_t)p.R};
+    cuuint64_t strides[2] = {row_bytes, row_bytes * p.Hq};
+    cuuint32_t box[3] = {64, (cuuint32_t)p.G, (cuuint32_t)(BM / p.G)};
+    if (!encode(&mq, p.q, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t rows = p.paged ? (cuuint64_t)p.num_pages * p.Hkv * kPageSize
+                                    : (cuuint64_t)p.B * p.Hkv * p.capacity;
+    cuuint64_t dims[2] = {(cuuint64_t)D, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {64, (cuuint32_t)(p.paged ? kPageSize : BN)};
+    if (!encode(&mkc, p.k_cache, 2, dims, strides, box) || !encode(&mvc, p.v_cache, 2, dims, strides, box))
+      return cudaErrorInvalidValue;
+  }
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)p.Hkv * p.R};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {64, BN};
+    if (!encode(&mkt, p.k_tree, 2, dims, strides, box) || !encode(&mvt, p.v_tree, 2, dims, strides, box))
+      return cudaErrorInvalidValue;
+  }
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(tv_attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)Cfg<D>::SMEM);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  dim3 grid(p.row_tiles, p.Hkv * p.splits, p.B);
+  tv_attn_tc_kernel<D><<<grid, 256, Cfg<D>::SMEM, st>>>(p, mq, mkc, mvc, mkt, mvt);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_supported(const tv_desc* d, int G) {
+  if (d->dtype != TV_BF16 || (d->head_dim != 128 && d->head_dim != 256)) return false;
+  if (G < 1 || G > BM) return false;
+  // TMA coordinates are int32: every row index must fit
+  const int64_t lim = ((int64_t)1 << 31) - 1;
+  const int64_t cache_rows = d->page_size ? d->num_pages * d->num_kv_heads * kPageSize
+                                          : (int64_t)d->batch * d->num_kv_heads * d->capacity;
+  if (cache_rows + BN > lim || (int64_t)d->num_kv_heads * d->total_rows + BN > lim) return false;
+  return true;
+}
+
+int tc_key_tile(int) { return BN; }
+
+cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t s) {
+  if (p.d == 128) return launch_tc_t<128>(p, s);
+  return launch_tc_t<256>(p, s);
+}
 
 }  // namespace tv

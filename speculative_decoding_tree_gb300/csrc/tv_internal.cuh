@@ -119,7 +119,7 @@ struct AcceptParams {
 cudaError_t launch_accept_commit(const AcceptParams& p, cudaStream_t s);
 
 // tcgen05 kernel availability for a descriptor (head_dim, group size).
-bool tc_supported(int d, int G, int dtype, int max_nodes);
+bool tc_supported(const tv_desc* d, int G);
 int tc_key_tile(int d);
 
 }  // namespace tv
