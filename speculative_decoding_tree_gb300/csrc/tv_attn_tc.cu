@@ -19,11 +19,12 @@
 //   warp 1      owns tensor memory; lane 0 issues tcgen05.mma:
 //               S(t) = Q K(t)^T into one of two 128-column TMEM buffers, then
 //               O += P(t-1) V(t-1) with P read from TMEM.
-//   warps 4-7   softmax, one thread per query row (its TMEM lane): load the
-//               S row, mask, running max, P = 2^(s*c - m) written back over
-//               the S columns as bf16 pairs, running sum; rescale the O row
-//               in TMEM only when the maximum grows by more than 2^8; at the
-//               end write the partial (O, m, l).
+//   warps 4-11  softmax, two threads per query row (its TMEM lane), each
+//               taking half of the tile's keys: load the S half-row, mask,
+//               exchange the half-row maxima, P = 2^(s*c - m) written back
+//               over the S columns as bf16 pairs, running sum; rescale the O
+//               row in TMEM only when the maximum grows by more than 2^8; at
+//               the end write the partial (O, m, l).
 //
 // Keys: the chunk's prefix positions in 128-key tiles, then (in the last
 // chunk of the sequence) one tile of the sequence's tree keys masked by the
@@ -52,6 +53,9 @@ constexpr uint32_t BOX_BYTES = BN * 128;        // one TMA box: 128 rows x 64 bf
 constexpr uint32_t CHUNK_BYTES = 2 * BOX_BYTES; // 128 keys x 128 columns
 constexpr uint64_t kWaitNs = 1000000000ull;
 constexpr float kRescaleThreshold = 8.0f;       // rescale O when the max grows by > 2^8
+constexpr int kThreads = 384;                   // warps 0 producer, 1 MMA, 2-3 idle, 4-11 softmax
+constexpr int kSoftmax = 256;                   // two warpgroups, each half of a row's keys
+constexpr uint32_t kHeader = 3072;              // barriers, TMEM address, row exchange (then 1 KB aligned)
 
 template <int D>
 struct Cfg {
@@ -59,8 +63,10 @@ struct Cfg {
   static constexpr int NS = D == 256 ? 5 : 6;     // ring slots
   static constexpr uint32_t Q_BYTES = BM * D * 2;
   static constexpr uint32_t RING_BYTES = NS * CHUNK_BYTES;
-  static constexpr int NBARS = 2 * NS + 9;
-  static constexpr uint32_t SMEM = 1024 + Q_BYTES + RING_BYTES + NBARS * 8 + 16;
+  static constexpr int NBARS = 2 * NS + 12;
+  static constexpr uint32_t SMEM = kHeader + Q_BYTES + RING_BYTES;
+  static_assert(NBARS * 8 + 8 <= 256, "barriers overflow the header");
+  static_assert(SMEM <= 232448, "shared memory over the 227 KB per-block limit");
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -75,13 +81,14 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(kThreads, 1)
 tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_vc,
                   const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_vt) {
   using C = Cfg<D>;
   constexpr int CPT = C::CPT, NS = C::NS;
-  extern __shared__ uint8_t smem_raw[];
+  constexpr unsigned kAll = 0xffffffffu;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
 
   // ---------------------------------------------------------------- work
   const int rt = blockIdx.x;
@@ -99,6 +106,11 @@ tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ 
   if (P != Praw && threadIdx.x == 0 && rt == 0 && s == 0 && g == 0) set_status(p.status, TV_DEV_BAD_PREFIX);
   const int nch = num_chunks(P, p.chunk);
   if (s >= nch) return;
+  // the layout below needs the dynamic shared window to start 1 KB aligned
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) set_status(p.status, TV_DEV_TIMEOUT);
+    return;
+  }
   const int64_t k_begin = (int64_t)s * p.chunk;
   const int64_t k_end = min(P, k_begin + p.chunk);
   const bool has_tree = (s == nch - 1);
@@ -107,21 +119,21 @@ tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ 
   const int tail_valid = npt > 0 ? (int)(k_end - (k_begin + (int64_t)(npt - 1) * BN)) : BN;
 
   // ---------------------------------------------------------------- smem
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = base;
-  uint8_t* ring = base + C::Q_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(ring + C::RING_BYTES);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBARS);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + C::NBARS * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* xch = reinterpret_cast<float*>(smem_raw + 256);        // [2 parity][2 half][128 rows]
+  uint8_t* sQ = smem_raw + kHeader;
+  uint8_t* ring = sQ + C::Q_BYTES;
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   auto FULL = [&](int i) { return bar(i); };
   auto EMPTY = [&](int i) { return bar(NS + i); };
-  const uint32_t Q_FULL = bar(2 * NS), S_FULL0 = bar(2 * NS + 1), P_FULL0 = bar(2 * NS + 3);
-  const uint32_t O_DONE0 = bar(2 * NS + 5), TAIL = bar(2 * NS + 7), FIN = bar(2 * NS + 8);
-  auto S_FULL = [&](int i) { return S_FULL0 + 8 * i; };   // QK(t) done, buffer t & 1
-  auto P_FULL = [&](int i) { return P_FULL0 + 8 * i; };   // softmax wrote P(t), buffer t & 1
-  auto O_DONE = [&](int i) { return O_DONE0 + 8 * i; };   // PV(t) done, alternating by t & 1
-  constexpr unsigned kAll = 0xffffffffu;
+  const int bq = 2 * NS;
+  const uint32_t Q_FULL = bar(bq), TAIL = bar(bq + 7), FIN = bar(bq + 8), XL = bar(bq + 11);
+  auto S_FULL = [&](int i) { return bar(bq + 1 + i); };   // QK(t) done, buffer t & 1
+  auto P_FULL = [&](int i) { return bar(bq + 3 + i); };   // softmax wrote P(t), buffer t & 1
+  auto O_DONE = [&](int i) { return bar(bq + 5 + i); };   // PV(t) done, alternating by t & 1
+  auto XCH = [&](int i) { return bar(bq + 9 + i); };      // row maxima exchanged for tile t, t & 1
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -130,14 +142,15 @@ tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ 
       mbar_init(EMPTY(i), 1);
     }
     mbar_init(Q_FULL, 1);
-    mbar_init(S_FULL(0), 1);
-    mbar_init(S_FULL(1), 1);
-    mbar_init(P_FULL(0), 128);
-    mbar_init(P_FULL(1), 128);
-    mbar_init(O_DONE(0), 1);
-    mbar_init(O_DONE(1), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(S_FULL(i), 1);
+      mbar_init(P_FULL(i), kSoftmax);
+      mbar_init(O_DONE(i), 1);
+      mbar_init(XCH(i), kSoftmax);
+    }
     mbar_init(TAIL, 1);
     mbar_init(FIN, 1);
+    mbar_init(XL, kSoftmax);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -165,6 +178,8 @@ tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ 
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_kc);
       tma_prefetch_desc(&tm_vc);
+      tma_prefetch_desc(&tm_kt);
+      tma_prefetch_desc(&tm_vt);
       mbar_expect_tx(Q_FULL, (uint32_t)p.rows_per_tile * 128u * (D / 64));
       for (int kb = 0; kb < D / 64; ++kb)
         tma_load_3d(smem_u32(sQ + kb * (BM * 128)), &tm_q, Q_FULL, kb * 64, g * G, o0 + m0 / G);
@@ -207,7 +222,7 @@ tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ 
               for (int pg = 0; pg < npages; ++pg) {
                 const int64_t pos = t0 + pg * kPageSize;
                 const int pid = p.page_table[(int64_t)b * p.max_pages + pos / kPageSize];
-                int row = oob_row;
+                int row = oob_row;                       // out of range: the copy reads zeros
                 if (pid >= 0 && pid < p.num_pages) {
                   row = (int)(((int64_t)pid * p.Hkv + g) * kPageSize);
                 } else if (c == 0) {
@@ -300,39 +315,58 @@ tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ 
     }
   } else if (warp >= 4) {
     // ============================================================ softmax
-    // Every tcgen05.ld / st below is warp-collective (.sync.aligned): control
-    // flow around them stays warp-uniform, per-row choices only pick values.
-    const int r = tid - 128;                                // row in the tile == TMEM lane
-    const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
+    // Two warpgroups: `half` 0 takes keys 0-63 of every tile (and O columns
+    // [0, D/2)), half 1 keys 64-127 (and O columns [D/2, D)); the two threads
+    // of a row share its running maximum through `xch`.  Every tcgen05.ld /
+    // st is warp-collective (.sync.aligned): control flow around them stays
+    // warp-uniform and per-row choices only pick values.
+    const int half = (tid - 128) >> 7;
+    const int r = (tid - 128) & 127;                        // row in the tile == TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const bool row_ok = r < p.rows_per_tile && (m0 + r) < nrows;
     const int node = (m0 + r) / G;
     const uint64_t anc = row_ok ? p.anc[o0 + node] : 0ull;
     const float c2 = p.scale_log2;
+    const int kofs = half * (BN / 2);                       // first key of this half
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int t = 0; t < T && ok; ++t) {
       if (!__all_sync(kAll, mbar_wait(S_FULL(t & 1), (t >> 1) & 1, abort_flag, kWaitNs))) { ok = false; break; }
       tc_fence_after();
       const uint32_t sbuf = tmem + lane_base + (uint32_t)((t & 1) * 128);
-      float sv[BN];
+      float sv[BN / 2];
+      {
+        uint32_t rr[64];
+        tmem_ld_x64(sbuf + kofs, rr);
 #pragma unroll
-      for (int q = 0; q < BN / 32; ++q) {
-        uint32_t rr[32];
-        tmem_ld_x32(sbuf + q * 32, rr);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) sv[q * 32 + e] = __uint_as_float(rr[e]);
+        for (int e = 0; e < 64; ++e) sv[e] = __uint_as_float(rr[e]);
       }
-      // mask: tree tile -> ancestor bits; partial last prefix tile -> key range
       const bool tree = (t == npt);
-      const int lim = tree ? min(n, 64) : ((t == npt - 1) ? tail_valid : BN);
-      float mx = -INFINITY;
+      const bool partial = tree || (t == npt - 1 && tail_valid < BN);
+      if (partial) {
+        // tree tile: ancestor bits; last prefix tile: key range
+        const int lim = tree ? min(n, 64) : tail_valid;
 #pragma unroll
-      for (int e = 0; e < BN; ++e) {
-        bool vis = e < lim;
-        if (tree) vis = vis && ((anc >> (e & 63)) & 1ull);
-        sv[e] = vis ? sv[e] : -INFINITY;
-        mx = fmaxf(mx, sv[e]);
+        for (int e = 0; e < 64; ++e) {
+          const int key = kofs + e;
+          bool vis = key < lim;
+          if (tree) vis = vis && ((anc >> (key & 63)) & 1ull);
+          sv[e] = vis ? sv[e] : -INFINITY;
+        }
       }
+      float mx8[8];
+#pragma unroll
+      for (int a = 0; a < 8; ++a) mx8[a] = sv[a];
+#pragma unroll
+      for (int e = 8; e < 64; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], sv[e]);
+      float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      // exchange the half-row maximum with the other half
+      float* xb = xch + (t & 1) * 256;
+      xb[half * 128 + r] = mx;
+      mbar_arrive(XCH(t & 1));
+      if (!__all_sync(kAll, mbar_wait(XCH(t & 1), (t >> 1) & 1, abort_flag, kWaitNs))) { ok = false; break; }
+      mx = fmaxf(mx, xb[(half ^ 1) * 128 + r]);
       const float m_tile = mx == -INFINITY ? -INFINITY : mx * c2;
       const float m_new = fmaxf(m_ref, m_tile);
       const bool first = (m_ref == -INFINITY);              // nothing accumulated yet
@@ -344,9 +378,9 @@ tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ 
         tc_fence_after();
         const float alpha = need ? ex2(m_ref - m_new) : 1.f;
 #pragma unroll 1
-        for (int q = 0; q < D / 32; ++q) {
+        for (int q = 0; q < D / 64; ++q) {
           uint32_t rr[32];
-          const uint32_t oa = tmem + lane_base + 256 + q * 32;
+          const uint32_t oa = tmem + lane_base + 256 + half * (D / 2) + q * 32;
           tmem_ld_x32(oa, rr);
 #pragma unroll
           for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
@@ -358,36 +392,42 @@ tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ 
         }
       }
       if (first) m_ref = m_new;
-      const bool live = m_ref != -INFINITY;
+      const float nm = m_ref == -INFINITY ? 0.f : -m_ref;   // masked keys: 2^-inf = 0
+      float l8[8];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pk[32];
+      for (int a = 0; a < 8; ++a) l8[a] = 0.f;
+      uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float x0 = sv[h * 64 + 2 * e], x1 = sv[h * 64 + 2 * e + 1];
-          const float p0 = live ? ex2(fmaf(x0, c2, -m_ref)) : 0.f;
-          const float p1 = live ? ex2(fmaf(x1, c2, -m_ref)) : 0.f;
-          l += p0 + p1;
-          pk[e] = pack_bf16(p0, p1);
-        }
-        tmem_st_x32(sbuf + h * 32, pk);
+      for (int e = 0; e < 32; ++e) {
+        const float p0 = ex2(fmaf(sv[2 * e], c2, nm));
+        const float p1 = ex2(fmaf(sv[2 * e + 1], c2, nm));
+        l8[(2 * e) & 7] += p0;
+        l8[(2 * e + 1) & 7] += p1;
+        pk[e] = pack_bf16(p0, p1);
       }
+      l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+      tmem_st_x32(sbuf + half * 32, pk);                   // P over the S columns, bf16 pairs
       tc_fence_before();
       mbar_arrive(P_FULL(t & 1));
     }
-    // epilogue: the last P V has landed (its commit covers every earlier MMA);
-    // write this chunk's partial
+    // epilogue: the last P V has landed (its commit covers every earlier
+    // MMA); add the two halves' sums; write this chunk's partial
     const int u = T - 1;
     if (ok && __all_sync(kAll, mbar_wait(O_DONE(u & 1), (u >> 1) & 1, abort_flag, kWaitNs))) {
       tc_fence_after();
+      float* xb = xch + (T & 1) * 256;
+      xb[half * 128 + r] = l;
+      mbar_arrive(XL);
+      const bool got = __all_sync(kAll, mbar_wait(XL, 0, abort_flag, kWaitNs));
+      const float lsum = l + xb[(half ^ 1) * 128 + r];
       const int64_t rowg = o0 + node;
       const int h = g * G + (m0 + r) % G;
       const int64_t idx = ((int64_t)s * p.R + rowg) * p.Hq + h;
-      float4* dst = reinterpret_cast<float4*>(p.o_part + idx * D);
+      float4* dst = reinterpret_cast<float4*>(p.o_part + idx * D + half * (D / 2));
 #pragma unroll 1
-      for (int q = 0; q < D / 32; ++q) {
+      for (int q = 0; q < D / 64; ++q) {
         uint32_t rr[32];
-        tmem_ld_x32(tmem + lane_base + 256 + q * 32, rr);
+        tmem_ld_x32(tmem + lane_base + 256 + half * (D / 2) + q * 32, rr);
         if (row_ok) {
 #pragma unroll
           for (int e = 0; e < 8; ++e)
@@ -395,7 +435,7 @@ tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ 
                                          __uint_as_float(rr[4 * e + 2]), __uint_as_float(rr[4 * e + 3]));
         }
       }
-      if (row_ok) p.ml_part[idx] = make_float2(m_ref, l);
+      if (row_ok && half == 0 && got) p.ml_part[idx] = make_float2(m_ref, lsum);
     }
   }
 
@@ -475,7 +515,7 @@ cudaError_t launch_tc_t(const AttnParams& p, cudaStream_t st) {
     configured = true;
   }
   dim3 grid(p.row_tiles, p.Hkv * p.splits, p.B);
-  tv_attn_tc_kernel<D><<<grid, 256, Cfg<D>::SMEM, st>>>(p, mq, mkc, mvc, mkt, mvt);
+  tv_attn_tc_kernel<D><<<grid, kThreads, Cfg<D>::SMEM, st>>>(p, mq, mkc, mvc, mkt, mvt);
   return cudaGetLastError();
 }
 
