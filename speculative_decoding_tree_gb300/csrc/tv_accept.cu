@@ -18,31 +18,35 @@ namespace {
 
 // ----------------------------------------------------------------- A0
 
-// One block per sequence, one thread per node: walk the parent chain.
+// One block per sequence, one thread per node: the sequence's parents are
+// read into shared memory in one step, then each thread walks its chain there.
 __global__ void tree_mask_kernel(const int32_t* __restrict__ parents, const int32_t* __restrict__ offs,
                                  uint64_t* __restrict__ anc, int32_t* __restrict__ depth, int32_t* status,
                                  int B, int R, int max_nodes) {
+  __shared__ int s_par[kMaxNodes];
   const int b = blockIdx.x;
   if (b == B - 1 && threadIdx.x == 0 && offs[B] != R) set_status(status, TV_DEV_BAD_OFFSETS);
   int o0, n;
-  if (!seq_rows(offs, b, R, max_nodes, status, &o0, &n)) return;
+  if (!seq_rows(offs, b, R, max_nodes, status, &o0, &n)) return;   // uniform over the block
   const int i = threadIdx.x;
+  if (i < n) s_par[i] = parents[o0 + i];
+  __syncthreads();
   if (i >= n) return;
   uint64_t bits = 0;
   int dep = 0, j = i;
   bool ok = true;
   while (true) {                       // terminates: the chain index strictly falls
     bits |= 1ull << j;
-    const int p = parents[o0 + j];
+    const int q = s_par[j];
     if (j == 0) {
-      ok = (p == -1);
+      ok = (q == -1);
       break;
     }
-    if (p < 0 || p >= j) {
+    if (q < 0 || q >= j) {
       ok = false;
       break;
     }
-    j = p;
+    j = q;
     ++dep;
   }
   if (!ok) {
@@ -70,60 +74,106 @@ __device__ __forceinline__ Best better(Best a, Best b) {
   return a.i <= b.i ? a : b;
 }
 
-__device__ __forceinline__ void consider(Best& bst, float x, int idx) {
-  if (x != x) return;                               // NaN
-  if (bst.i < 0 || x > bst.v || (x == bst.v && idx < bst.i)) {
-    bst.v = x;
-    bst.i = idx;
-  }
-}
-
 template <bool BF16>
 __device__ __forceinline__ float load_elem(const void* base, int64_t e) {
   if (BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[e]);
   return reinterpret_cast<const float*>(base)[e];
 }
 
-// grid (vchunks, R): block reduces one vocab chunk of one row with 16-byte
-// loads over the aligned body and scalar loads at the ragged ends.
+// In-order update: a thread sees its elements in increasing index order, so
+// a strictly greater value is the only way to replace the current best (ties
+// keep the earlier, smaller index); NaN never enters; the first non-NaN value
+// is taken even when it is -inf.
+__device__ __forceinline__ void take_in_order(Best& bst, float x, int idx) {
+  const bool take = (x > bst.v) || (bst.i < 0 && x == x);
+  bst.v = take ? x : bst.v;
+  bst.i = take ? idx : bst.i;
+}
+
+// Largest of the 8 values in a 16-byte word (NaN ignored unless all are NaN).
+template <bool BF16>
+__device__ __forceinline__ float vec_max(const uint4& u) {
+  if (BF16) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+    const __nv_bfloat162 m = __hmax2(__hmax2(h[0], h[1]), __hmax2(h[2], h[3]));
+    return fmaxf(__low2float(m), __high2float(m));
+  }
+  const float* f = reinterpret_cast<const float*>(&u);
+  return fmaxf(fmaxf(f[0], f[1]), fmaxf(f[2], f[3]));
+}
+
+// First element of the word equal to `x` (x is a value the word holds).
+template <bool BF16>
+__device__ __forceinline__ int vec_first(const uint4& u, float x) {
+  if (BF16) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      if (__low2float(h[t]) == x) return 2 * t;
+      if (__high2float(h[t]) == x) return 2 * t + 1;
+    }
+    return 7;
+  }
+  const float* f = reinterpret_cast<const float*>(&u);
+#pragma unroll
+  for (int t = 0; t < 3; ++t)
+    if (f[t] == x) return t;
+  return 3;
+}
+
+// grid (vchunks, R): one block reduces one vocab chunk of one row.  Each
+// thread streams 16-byte words (four in flight) in increasing index order.
+// A packed max over each batch of words is compared with the thread's best:
+// only a strictly larger batch maximum triggers the index search (first
+// word, then first element, holding it), so equal values keep the earlier
+// index and NaN never wins.  Scalar loads cover the ragged chunk ends.
 template <bool BF16>
 __global__ __launch_bounds__(256) void argmax_partial_kernel(const void* __restrict__ logits, int V, int vlen,
                                                              int vchunks, float* __restrict__ am_val,
                                                              int32_t* __restrict__ am_idx) {
   constexpr int ES = BF16 ? 2 : 4;
   constexpr int PER = 16 / ES;                       // elements per 16-byte load
+  constexpr int UNROLL = 4;
   const int row = blockIdx.y, c = blockIdx.x;
   const int v0 = c * vlen;
   const int v1 = min(V, v0 + vlen);
   const int64_t rbase = (int64_t)row * V;            // element index of the row start
-  Best bst{-FLT_MAX, -1};
-  // first element index >= v0 whose address is 16-byte aligned
   const uintptr_t addr0 = reinterpret_cast<uintptr_t>(logits) + (uintptr_t)((rbase + v0) * ES);
   int head = (int)(((16 - (addr0 & 15)) & 15) / ES);
   if ((addr0 & (ES - 1)) != 0) head = v1 - v0;       // cannot align: all scalar
-  int a0 = min(v0 + head, v1);
-  int nvec = (v1 - a0) / PER;
-  int a1 = a0 + nvec * PER;
-  for (int e = v0 + threadIdx.x; e < a0; e += blockDim.x) consider(bst, load_elem<BF16>(logits, rbase + e), e);
+  const int a0 = min(v0 + head, v1);
+  const int nvec = (v1 - a0) / PER;
+  const int a1 = a0 + nvec * PER;
+  Best bst{-INFINITY, -1};
+  // head (lowest indices) first, then the body, then the tail: in order
+  for (int e = v0 + (int)threadIdx.x; e < a0; e += blockDim.x) take_in_order(bst, load_elem<BF16>(logits, rbase + e), e);
   const uint4* vp = reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(logits) + (rbase + a0) * ES);
-  for (int k = threadIdx.x; k < nvec; k += blockDim.x) {
-    uint4 u = __ldcs(vp + k);                        // streamed once: do not keep in L1
-    const int e0 = a0 + k * PER;
-    if (BF16) {
-      const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+  const int step = (int)blockDim.x;
+  for (int k0 = threadIdx.x; k0 < nvec; k0 += UNROLL * step) {
+    uint4 u[UNROLL];
+    float m[UNROLL];
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        float2 f = __bfloat1622float2(h2[t]);
-        consider(bst, f.x, e0 + 2 * t);
-        consider(bst, f.y, e0 + 2 * t + 1);
-      }
-    } else {
-      const float* f = reinterpret_cast<const float*>(&u);
+    for (int q = 0; q < UNROLL; ++q) {
+      const int k = k0 + q * step;
+      u[q] = k < nvec ? __ldcs(vp + k) : make_uint4(0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu);
+    }
 #pragma unroll
-      for (int t = 0; t < 4; ++t) consider(bst, f[t], e0 + t);
+    for (int q = 0; q < UNROLL; ++q) m[q] = (k0 + q * step < nvec) ? vec_max<BF16>(u[q]) : __int_as_float(0x7fffffff);
+    const float mb = fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));    // NaN only if all NaN
+    if (mb > bst.v || (bst.i < 0 && mb == mb)) {
+      int qs = UNROLL - 1;                          // first word holding the batch maximum
+#pragma unroll
+      for (int q = UNROLL - 1; q >= 0; --q)
+        if (m[q] == mb) qs = q;
+      uint4 uq = u[0];
+#pragma unroll
+      for (int q = 1; q < UNROLL; ++q)
+        if (q == qs) uq = u[q];
+      bst.v = mb;
+      bst.i = a0 + (k0 + qs * step) * PER + vec_first<BF16>(uq, mb);
     }
   }
-  for (int e = a1 + threadIdx.x; e < v1; e += blockDim.x) consider(bst, load_elem<BF16>(logits, rbase + e), e);
+  for (int e = a1 + (int)threadIdx.x; e < v1; e += blockDim.x) take_in_order(bst, load_elem<BF16>(logits, rbase + e), e);
   // warp then block reduction
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
@@ -146,17 +196,19 @@ __global__ __launch_bounds__(256) void argmax_partial_kernel(const void* __restr
 
 // ----------------------------------------------------------------- A4 + A5
 
-// One block per sequence: finish the argmax, walk, then copy the accepted
-// rows' K/V into the cache and advance prefix_len.
+// One block per sequence.  Warp 0 finishes the argmax of every node, builds
+// ancestors and depths, and walks (lane i owns nodes i and i + 32; ballots
+// and shuffles, no shared atomics); then the whole block copies the accepted
+// rows' K/V into the cache and advances prefix_len.
 __global__ __launch_bounds__(256) void walk_commit_kernel(AcceptParams p) {
-  __shared__ int s_am[kMaxNodes], s_par[kMaxNodes], s_draft[kMaxNodes], s_dep[kMaxNodes];
+  __shared__ int s_par[kMaxNodes], s_draft[kMaxNodes], s_am[kMaxNodes], s_path[kMaxNodes];
   __shared__ uint64_t s_anc[kMaxNodes];
-  __shared__ unsigned long long s_match;
-  __shared__ int s_bad_tree, s_key, s_commit_ok, s_P;
-  __shared__ int s_path[kMaxNodes];
+  __shared__ float s_pv[kMaxNodes * kMaxVChunks];
+  __shared__ int s_pi[kMaxNodes * kMaxVChunks];
+  __shared__ int s_P, s_k, s_ok;
 
   const int b = blockIdx.x;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int o0, n;
   if (!seq_rows(p.node_offsets, b, p.R, p.max_nodes, p.status, &o0, &n)) {
     if (tid < p.max_nodes) {
@@ -166,131 +218,173 @@ __global__ __launch_bounds__(256) void walk_commit_kernel(AcceptParams p) {
     if (tid == 0) p.accept_len[b] = -1;
     return;
   }
-  if (tid == 0) {
-    s_match = 0ull;
-    s_bad_tree = 0;
-    s_key = -1;
+  // every global read the walk needs, issued together
+  const int vc = p.vchunks;
+  if (tid == 0) s_P = p.prefix_len[b];
+  if (tid < n) {
+    s_par[tid] = p.parents[o0 + tid];
+    s_draft[tid] = p.draft[o0 + tid];
+  }
+  for (int e = tid; e < n * vc; e += blockDim.x) {
+    s_pv[e] = p.am_val[(int64_t)o0 * vc + e];
+    s_pi[e] = p.am_idx[(int64_t)o0 * vc + e];
   }
   __syncthreads();
 
-  // finish the argmax of each row from its chunk partials (ascending chunk
-  // order keeps the smallest index on ties)
-  if (tid < n) {
-    Best bst{-FLT_MAX, -1};
-    const int64_t r = o0 + tid;
-    for (int c = 0; c < p.vchunks; ++c) {
-      Best o{p.am_val[r * p.vchunks + c], p.am_idx[r * p.vchunks + c]};
-      bst = better(bst, o);
+  if (warp == 0) {
+    const unsigned all = 0xffffffffu;
+    // argmax of each node from its chunk partials (ascending chunk order
+    // keeps the smallest index on ties)
+#pragma unroll
+    for (int hlf = 0; hlf < 2; ++hlf) {
+      const int i = lane + 32 * hlf;
+      if (i < n) {
+        Best bst{-FLT_MAX, -1};
+        for (int c = 0; c < vc; ++c) bst = better(bst, Best{s_pv[i * vc + c], s_pi[i * vc + c]});
+        const int am = bst.i < 0 ? 0 : bst.i;
+        s_am[i] = am;
+        p.argmax[o0 + i] = am;
+      }
     }
-    const int am = bst.i < 0 ? 0 : bst.i;
-    s_am[tid] = am;
-    p.argmax[r] = am;
-    s_par[tid] = p.parents[r];
-    s_draft[tid] = p.draft[r];
-  }
-  __syncthreads();
-
-  // ancestors and depth by walking parents; validate the tree
-  if (tid < n) {
-    uint64_t bits = 0;
-    int dep = 0, j = tid;
+    __syncwarp();
+    // ancestors and depth by walking parents; validate; match against the
+    // parent's argmax
+    uint64_t anc[2] = {0ull, 0ull};
+    int dep[2] = {0, 0};
+    bool mt[2] = {false, false}, bad = false;
+#pragma unroll
+    for (int hlf = 0; hlf < 2; ++hlf) {
+      const int i = lane + 32 * hlf;
+      if (i < n) {
+        uint64_t bits = 0;
+        int d = 0, j = i;
+        bool ok = true;
+        while (true) {                              // terminates: the chain index strictly falls
+          bits |= 1ull << j;
+          const int q = s_par[j];
+          if (j == 0) {
+            ok = (q == -1);
+            break;
+          }
+          if (q < 0 || q >= j) {
+            ok = false;
+            break;
+          }
+          j = q;
+          ++d;
+        }
+        if (!ok) {
+          bad = true;
+          bits = 1ull << i;
+          d = 0;
+        }
+        anc[hlf] = bits;
+        dep[hlf] = d;
+        s_anc[i] = bits;
+        mt[hlf] = (i == 0) || (ok && s_draft[i] == s_am[s_par[i]]);
+      }
+    }
+    if (__any_sync(all, bad) && lane == 0) set_status(p.status, TV_DEV_BAD_TREE);
+    const uint64_t match = (uint64_t)__ballot_sync(all, mt[0]) | ((uint64_t)__ballot_sync(all, mt[1]) << 32);
+    // reachable = every node on the root path matches; best = deepest, then
+    // smallest index
+    int key = -1;
+#pragma unroll
+    for (int hlf = 0; hlf < 2; ++hlf) {
+      const int i = lane + 32 * hlf;
+      if (i < n && (anc[hlf] & ~match) == 0) key = max(key, (dep[hlf] << 8) | (255 - i));
+    }
+    key = __reduce_max_sync(all, key);              // >= 0: the root is always reachable
+    const int end = 255 - (key & 255), k = key >> 8;
+    __syncwarp();
+    const uint64_t end_anc = s_anc[end];
+#pragma unroll
+    for (int hlf = 0; hlf < 2; ++hlf) {
+      const int i = lane + 32 * hlf;
+      if (i < n && ((end_anc >> i) & 1ull)) s_path[dep[hlf]] = i;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int hlf = 0; hlf < 2; ++hlf) {
+      const int t = lane + 32 * hlf;
+      if (t < p.max_nodes) {
+        const int64_t o = (int64_t)b * p.max_nodes + t;
+        p.path[o] = t <= k ? s_path[t] : -1;
+        p.tokens[o] = t < k ? s_draft[s_path[t + 1]] : (t == k ? s_am[end] : -1);
+      }
+    }
+    // can the k+1 rows be committed?
+    const int P = s_P;
     bool ok = true;
-    while (true) {
-      bits |= 1ull << j;
-      const int q = s_par[j];
-      if (j == 0) {
-        ok = (q == -1);
-        break;
-      }
-      if (q < 0 || q >= j) {
-        ok = false;
-        break;
-      }
-      j = q;
-      ++dep;
-    }
-    if (!ok) {
-      s_bad_tree = 1;
-      bits = 1ull << tid;
-      dep = 0;
-    }
-    s_anc[tid] = bits;
-    s_dep[tid] = dep;
-    // node matches when its draft equals the target argmax at its parent
-    const bool m = (tid == 0) || (ok && s_draft[tid] == s_am[s_par[tid]]);
-    if (m) atomicOr(&s_match, 1ull << tid);
-  }
-  __syncthreads();
-  if (s_bad_tree && tid == 0) set_status(p.status, TV_DEV_BAD_TREE);
-  // a node is reachable when every node on its root path matches; the best
-  // end is the deepest reachable node, ties to the smallest index
-  if (tid < n) {
-    const bool ok = (s_anc[tid] & ~(uint64_t)s_match) == 0;
-    if (ok) atomicMax(&s_key, (s_dep[tid] << 8) | (255 - tid));
-  }
-  __syncthreads();
-  const int key = s_key;                 // >= 0: the root is always reachable
-  const int end = 255 - (key & 255);
-  const int k = key >> 8;
-  if (tid < n && ((s_anc[end] >> tid) & 1ull)) s_path[s_dep[tid]] = tid;
-  __syncthreads();
-  if (tid < p.max_nodes) {
-    const int64_t o = (int64_t)b * p.max_nodes + tid;
-    p.path[o] = tid <= k ? s_path[tid] : -1;
-    p.tokens[o] = tid < k ? s_draft[s_path[tid + 1]] : (tid == k ? s_am[end] : -1);
-  }
-  if (tid == 0) {
-    p.accept_len[b] = k;
-    const int P = p.prefix_len[b];
-    s_P = P;
-    int ok = 1;
     if (P < 0) {
-      set_status(p.status, TV_DEV_BAD_PREFIX);
-      ok = 0;
+      ok = false;
+      if (lane == 0) set_status(p.status, TV_DEV_BAD_PREFIX);
     } else if ((int64_t)P + k + 1 > p.capacity) {
-      set_status(p.status, TV_DEV_CAPACITY);
-      ok = 0;
+      ok = false;
+      if (lane == 0) set_status(p.status, TV_DEV_CAPACITY);
+    } else if (p.paged) {
+      bool page_bad = false;
+#pragma unroll
+      for (int hlf = 0; hlf < 2; ++hlf) {
+        const int t = lane + 32 * hlf;
+        if (t <= k) {
+          const int64_t pos = (int64_t)P + t;
+          const int pid = p.page_table[(int64_t)b * p.max_pages + pos / kPageSize];
+          page_bad |= (pid < 0 || pid >= p.num_pages);
+        }
+      }
+      if (__any_sync(all, page_bad)) {
+        ok = false;
+        if (lane == 0) set_status(p.status, TV_DEV_BAD_PAGE);
+      }
     }
-    s_commit_ok = ok;
+    if (lane == 0) {
+      p.accept_len[b] = k;
+      s_k = k;
+      s_ok = ok ? 1 : 0;
+    }
   }
   __syncthreads();
-  if (!s_commit_ok) return;
-  const int P = s_P;
-  if (p.paged) {
-    // every page the commit writes must be valid before anything is written
-    if (tid <= k) {
-      const int64_t pos = (int64_t)P + tid;
-      const int pid = p.page_table[(int64_t)b * p.max_pages + pos / kPageSize];
-      if (pid < 0 || pid >= p.num_pages) s_commit_ok = 0;
-    }
-    __syncthreads();
-    if (!s_commit_ok) {
-      if (tid == 0) set_status(p.status, TV_DEV_BAD_PAGE);
-      return;
-    }
-  }
-  // copy k+1 rows x Hkv heads of K and of V in 16-byte units
+  if (!s_ok) return;
+  const int P = s_P, k = s_k;
+  // copy k+1 rows x Hkv heads of K and of V in 16-byte units: each thread
+  // loads all its units first, then stores them (the loads do not wait on
+  // the stores, which the compiler cannot prove independent)
   const int units_row = p.d * p.esize / 16;
-  const int64_t total = 2LL * (k + 1) * p.Hkv * units_row;
-  for (int64_t u = tid; u < total; u += blockDim.x) {
-    int64_t x = u;
-    const int cu = (int)(x % units_row); x /= units_row;
-    const int g = (int)(x % p.Hkv); x /= p.Hkv;
-    const int t = (int)(x % (k + 1)); x /= (k + 1);
-    const int which = (int)x;                     // 0 = K, 1 = V
-    const int node = s_path[t];
-    const char* src = reinterpret_cast<const char*>(which ? p.v_tree : p.k_tree) +
-                      (((int64_t)g * p.R + o0 + node) * p.d) * p.esize;
-    const int64_t pos = (int64_t)P + t;
-    int64_t drow;
-    if (p.paged) {
-      const int pid = p.page_table[(int64_t)b * p.max_pages + pos / kPageSize];
-      drow = ((int64_t)pid * p.Hkv + g) * kPageSize + pos % kPageSize;
-    } else {
-      drow = ((int64_t)b * p.Hkv + g) * p.capacity + pos;
+  const int per_kind = (k + 1) * p.Hkv;
+  const int total = 2 * per_kind * units_row;
+  constexpr int U = 8;
+  for (int base = 0; base < total; base += U * (int)blockDim.x) {
+    uint4 v[U];
+    uint4* dst[U];
+#pragma unroll
+    for (int q = 0; q < U; ++q) {
+      const int u = base + q * (int)blockDim.x + tid;
+      dst[q] = nullptr;
+      if (u < total) {
+        const int rr = u / units_row, cu = u - rr * units_row;
+        const int which = rr / per_kind;            // 0 = K, 1 = V
+        const int rem = rr - which * per_kind;
+        const int t = rem / p.Hkv, g = rem - t * p.Hkv;
+        const int node = s_path[t];
+        const uint4* src = reinterpret_cast<const uint4*>(
+            reinterpret_cast<const char*>(which ? p.v_tree : p.k_tree) + (((int64_t)g * p.R + o0 + node) * p.d) * p.esize);
+        const int64_t pos = (int64_t)P + t;
+        int64_t drow;
+        if (p.paged) {
+          const int pid = p.page_table[(int64_t)b * p.max_pages + pos / kPageSize];
+          drow = ((int64_t)pid * p.Hkv + g) * kPageSize + pos % kPageSize;
+        } else {
+          drow = ((int64_t)b * p.Hkv + g) * p.capacity + pos;
+        }
+        v[q] = src[cu];
+        dst[q] = reinterpret_cast<uint4*>(reinterpret_cast<char*>(which ? p.v_cache : p.k_cache) +
+                                          drow * p.d * p.esize) + cu;
+      }
     }
-    char* dst = reinterpret_cast<char*>(which ? p.v_cache : p.k_cache) + drow * p.d * p.esize;
-    reinterpret_cast<uint4*>(dst)[cu] = reinterpret_cast<const uint4*>(src)[cu];
+#pragma unroll
+    for (int q = 0; q < U; ++q)
+      if (dst[q]) *dst[q] = v[q];
   }
   __syncthreads();
   if (tid == 0) p.prefix_len[b] = P + k + 1;

@@ -82,10 +82,18 @@ int make_plan(const tv_desc* d, Plan* p) {
   int row_tiles = (d->max_nodes * G + rows_per_tile - 1) / rows_per_tile;
   int64_t units = (int64_t)d->batch * d->num_kv_heads * row_tiles;
   int64_t sms = num_sms();
-  int64_t want = (sms * (d->batch > 1 ? 4 : 1)) / units;
-  if (want < 1) want = 1;
   int64_t L = d->max_prefix;
-  int64_t chunk = (L + want - 1) / want;
+  int64_t chunk;
+  if (d->batch == 1) {
+    // one wave: the prefix split evenly over the SMs
+    int64_t want = sms / units;
+    if (want < 1) want = 1;
+    chunk = (L + want - 1) / want;
+  } else {
+    // ragged batch: fixed 1024-key chunks (about 8 key tiles) so that the
+    // block scheduler balances sequences of different lengths
+    chunk = 1024;
+  }
   chunk = align_up(chunk < 1 ? 1 : chunk, key_tile);
   if (chunk > (int64_t)1 << 30) return TV_ERR_OVERFLOW;
   int splits = num_chunks(L, (int)chunk);
@@ -107,16 +115,22 @@ int make_plan(const tv_desc* d, Plan* p) {
   return TV_OK;
 }
 
+// Vocabulary chunks per row for the argmax pass: about 16K elements per
+// block, but at least ~4 blocks per SM over all rows, never below 2K
+// elements per block and never more than kMaxVChunks chunks.
 void accept_chunks(int R, int V, int* vchunks, int* vchunk_len) {
-  int sms = num_sms();
-  int want = (2 * sms + R - 1) / R;
-  int maxc = (V + 4095) / 4096;
+  const int64_t sms = num_sms();
+  int64_t want = (V + 16383) / 16384;
+  const int64_t fill = (4 * sms + R - 1) / R;
+  if (fill > want) want = fill;
+  int64_t maxc = (V + 2047) / 2048;
+  if (maxc > kMaxVChunks) maxc = kMaxVChunks;
   if (want > maxc) want = maxc;
   if (want < 1) want = 1;
-  int len = (V + want - 1) / want;
+  int64_t len = (V + want - 1) / want;
   len = (len + 7) / 8 * 8;
-  *vchunk_len = len;
-  *vchunks = (V + len - 1) / len;
+  *vchunk_len = (int)len;
+  *vchunks = (int)((V + len - 1) / len);
 }
 
 int64_t accept_bytes(const tv_desc* d, int V) {
@@ -149,6 +163,8 @@ AttnParams attn_params(const tv_desc* d, const Plan& pl, const void* q, const vo
   a.prefix_len = plen; a.node_offsets = no; a.k_tree = kt; a.v_tree = vt; a.anc = anc;
   a.o_part = reinterpret_cast<float*>(ws);
   a.ml_part = reinterpret_cast<float2*>(reinterpret_cast<char*>(ws) + pl.o_part_bytes);
+  a.out = nullptr;
+  a.out_bf16 = (d->dtype == TV_BF16 && !d->out_f32) ? 1 : 0;
   a.status = st;
   a.B = d->batch; a.Hq = d->num_q_heads; a.Hkv = d->num_kv_heads; a.G = pl.G; a.d = d->head_dim;
   a.R = d->total_rows; a.max_nodes = d->max_nodes;
@@ -169,8 +185,9 @@ int launch_partials(const tv_desc* d, const Plan& pl, const AttnParams& a, cudaS
 }
 
 int launch_merge_from(const tv_desc* d, const Plan& pl, const int32_t* plen, const int32_t* no, void* out,
-                      const void* ws, int32_t* st, cudaStream_t s) {
+                      const void* ws, int32_t* st, cudaStream_t s, int skip_single) {
   MergeParams m;
+  m.skip_single = skip_single;
   m.prefix_len = plen; m.node_offsets = no;
   m.o_part = reinterpret_cast<const float*>(ws);
   m.ml_part = reinterpret_cast<const float2*>(reinterpret_cast<const char*>(ws) + pl.o_part_bytes);
@@ -286,7 +303,7 @@ int tv_attn_merge(const tv_desc* desc, const int32_t* d_prefix_len, const int32_
   if (rc) return rc;
   if ((int64_t)workspace_bytes < p.o_part_bytes + p.ml_part_bytes) return TV_ERR_WORKSPACE;
   return launch_merge_from(desc, p, d_prefix_len, d_node_offsets, d_out, d_workspace, d_status,
-                           as_stream(stream));
+                           as_stream(stream), 0);
 }
 
 int tree_verify_attn(const tv_desc* desc, const void* d_q, const void* d_k_cache, const void* d_v_cache,
@@ -306,10 +323,12 @@ int tree_verify_attn(const tv_desc* desc, const void* d_q, const void* d_k_cache
   if ((int64_t)workspace_bytes < p.o_part_bytes + p.ml_part_bytes) return TV_ERR_WORKSPACE;
   AttnParams a = attn_params(desc, p, d_q, d_k_cache, d_v_cache, d_page_table, d_prefix_len, d_node_offsets,
                              d_k_tree, d_v_tree, d_anc, d_workspace, d_status);
+  a.out = d_out;                      // one-chunk sequences are finished by the split pass
   cudaStream_t s = as_stream(stream);
   rc = launch_partials(desc, p, a, s);
   if (rc) return rc;
-  return launch_merge_from(desc, p, d_prefix_len, d_node_offsets, d_out, d_workspace, d_status, s);
+  if (p.pub.num_splits == 1) return TV_OK;   // every sequence has one chunk: nothing to merge
+  return launch_merge_from(desc, p, d_prefix_len, d_node_offsets, d_out, d_workspace, d_status, s, 1);
 }
 
 int tree_accept_commit(const tv_desc* desc, int32_t vocab, int32_t logits_dtype, const void* d_logits,

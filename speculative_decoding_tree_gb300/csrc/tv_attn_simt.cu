@@ -232,7 +232,9 @@ __global__ __launch_bounds__(128) void attn_simt_kernel(AttnParams p) {
     __syncwarp();
   }
 
-  // partial outputs of this split
+  // partial outputs of this split; a sequence with one chunk writes its
+  // normalised rows directly (the merge's arithmetic for one split)
+  const bool direct = p.out != nullptr && nch == 1;
 #pragma unroll
   for (int r = 0; r < RPW; ++r) {
     const int m = m0 + warp * RPW + r;
@@ -240,6 +242,25 @@ __global__ __launch_bounds__(128) void attn_simt_kernel(AttnParams p) {
     const int64_t rowg = o0 + m / p.G;
     const int h = g * p.G + m % p.G;
     const int64_t idx = ((int64_t)s * p.R + rowg) * p.Hq + h;
+    if (direct) {
+      const float inv = l_run[r] > 0.f ? 1.f / l_run[r] : 0.f;
+      const int64_t obase = (rowg * p.Hq + h) * D;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) {
+        const float4 v = make_float4(acc[r][c].x * inv, acc[r][c].y * inv, acc[r][c].z * inv, acc[r][c].w * inv);
+        const int64_t e = obase + (lane + 32 * c) * 4;
+        if (p.out_bf16) {
+          __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), bb = __floats2bfloat162_rn(v.z, v.w);
+          uint2 u;
+          u.x = *reinterpret_cast<uint32_t*>(&a);
+          u.y = *reinterpret_cast<uint32_t*>(&bb);
+          *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) + e) = u;
+        } else {
+          *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + e) = v;
+        }
+      }
+      continue;
+    }
     float4* dst = reinterpret_cast<float4*>(p.o_part + idx * D);
 #pragma unroll
     for (int c = 0; c < CPL; ++c) dst[lane + 32 * c] = acc[r][c];
@@ -247,12 +268,21 @@ __global__ __launch_bounds__(128) void attn_simt_kernel(AttnParams p) {
   }
 }
 
-// One warp per (row, head): combine the splits of the row's sequence.
+// Combine the splits of every (row, head): one thread per 16-byte column
+// chunk of the output (D/4 threads per pair), so the partial rows of all
+// splits stream in parallel across the GPU.  In each warp, lane s reads split
+// s's (m, l), so the maxima and weights cost one round trip; the O loads of
+// up to 8 splits are then issued together.  More than 32 splits take
+// several passes with a running maximum.
 template <int D>
-__global__ __launch_bounds__(128) void merge_kernel(MergeParams p) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t pair = (int64_t)blockIdx.x * 4 + warp;
-  if (pair >= (int64_t)p.R * p.Hq) return;
+__global__ __launch_bounds__(256, 2) void merge_kernel(MergeParams p) {
+  constexpr int TPP = D / 4;                       // threads per (row, head), a multiple of 32
+  constexpr int PPB = 256 / TPP;                   // pairs per block
+  constexpr int PF = 8;                            // O loads in flight per thread
+  const int lane = threadIdx.x & 31;
+  const int64_t pair = (int64_t)blockIdx.x * PPB + threadIdx.x / TPP;
+  const int c = threadIdx.x % TPP;
+  if (pair >= (int64_t)p.R * p.Hq) return;         // uniform over each warp (TPP % 32 == 0)
   const int row = (int)(pair / p.Hq);
   const int h = (int)(pair % p.Hq);
   // sequence of this row: node_offsets is non-decreasing when valid
@@ -265,45 +295,56 @@ __global__ __launch_bounds__(128) void merge_kernel(MergeParams p) {
   const bool valid = p.node_offsets[b] <= row && row < p.node_offsets[b + 1];
   const int64_t P = clamp_prefix(p.prefix_len[b], p.max_prefix, p.capacity);
   const int nch = valid ? num_chunks(P, p.chunk) : 0;
-  float M = -INFINITY;
-  for (int s = 0; s < nch; ++s) M = fmaxf(M, p.ml_part[((int64_t)s * p.R + row) * p.Hq + h].x);
-  constexpr int CPL = D / 128;
-  float4 acc[CPL];
+  if (p.skip_single && nch == 1) return;           // the split pass wrote this row (uniform per pair)
+  const int64_t stride = (int64_t)p.R * p.Hq;      // between splits, in (row, head) pairs
+  const float2* ml = p.ml_part + (int64_t)row * p.Hq + h;
+  const float4* op = reinterpret_cast<const float4*>(p.o_part) + ((int64_t)row * p.Hq + h) * (D / 4) + c;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float L = 0.f, Mrun = -INFINITY;
+  for (int s0 = 0; s0 < nch; s0 += 32) {
+    const int ns = min(32, nch - s0);
+    const float2 mine = lane < ns ? ml[(int64_t)(s0 + lane) * stride] : make_float2(-INFINITY, 0.f);
+    float Mp = mine.x;
 #pragma unroll
-  for (int c = 0; c < CPL; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-  float L = 0.f;
-  if (M != -INFINITY) {
-    for (int s = 0; s < nch; ++s) {
-      const int64_t idx = ((int64_t)s * p.R + row) * p.Hq + h;
-      const float2 ml = p.ml_part[idx];
-      const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
-      L += ml.y * w;
-      const float4* src = reinterpret_cast<const float4*>(p.o_part + idx * D);
+    for (int off = 16; off > 0; off >>= 1) Mp = fmaxf(Mp, __shfl_xor_sync(0xffffffffu, Mp, off));
+    const float Mnew = fmaxf(Mrun, Mp);
+    if (Mnew == -INFINITY) continue;               // every key so far masked
+    const float keep = Mrun == -INFINITY ? 0.f : exp2f(Mrun - Mnew);
+    acc.x *= keep; acc.y *= keep; acc.z *= keep; acc.w *= keep;
+    const float w = mine.x == -INFINITY ? 0.f : exp2f(mine.x - Mnew);
+    float lw = mine.y * w;
 #pragma unroll
-      for (int c = 0; c < CPL; ++c) {
-        const float4 v = src[lane + 32 * c];
-        acc[c].x = fmaf(w, v.x, acc[c].x);
-        acc[c].y = fmaf(w, v.y, acc[c].y);
-        acc[c].z = fmaf(w, v.z, acc[c].z);
-        acc[c].w = fmaf(w, v.w, acc[c].w);
+    for (int off = 16; off > 0; off >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, off);
+    L = L * keep + lw;
+    Mrun = Mnew;
+    for (int t0 = 0; t0 < ns; t0 += PF) {
+      float4 v[PF];
+#pragma unroll
+      for (int t = 0; t < PF; ++t)
+        if (t0 + t < ns) v[t] = op[(int64_t)(s0 + t0 + t) * stride * (D / 4)];
+#pragma unroll
+      for (int t = 0; t < PF; ++t) {
+        const float wt = __shfl_sync(0xffffffffu, w, (t0 + t) & 31);
+        if (t0 + t < ns) {
+          acc.x = fmaf(wt, v[t].x, acc.x);
+          acc.y = fmaf(wt, v[t].y, acc.y);
+          acc.z = fmaf(wt, v[t].z, acc.z);
+          acc.w = fmaf(wt, v[t].w, acc.w);
+        }
       }
     }
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
-  const int64_t obase = ((int64_t)row * p.Hq + h) * D;
-#pragma unroll
-  for (int c = 0; c < CPL; ++c) {
-    const float4 v = make_float4(acc[c].x * inv, acc[c].y * inv, acc[c].z * inv, acc[c].w * inv);
-    const int64_t e = obase + (lane + 32 * c) * 4;
-    if (p.out_bf16) {
-      __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), bb = __floats2bfloat162_rn(v.z, v.w);
-      uint2 u;
-      u.x = *reinterpret_cast<uint32_t*>(&a);
-      u.y = *reinterpret_cast<uint32_t*>(&bb);
-      *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) + e) = u;
-    } else {
-      *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + e) = v;
-    }
+  const float4 v = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  const int64_t e = ((int64_t)row * p.Hq + h) * D + c * 4;
+  if (p.out_bf16) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), bb = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&bb);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) + e) = u;
+  } else {
+    *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + e) = v;
   }
 }
 
@@ -339,10 +380,11 @@ cudaError_t launch_attn_simt(const AttnParams& p, int dtype, cudaStream_t s) {
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s) {
   const int64_t pairs = (int64_t)p.R * p.Hq;
-  const int blocks = (int)((pairs + 3) / 4);
-  if (p.d == 128) merge_kernel<128><<<blocks, 128, 0, s>>>(p);
-  else if (p.d == 256) merge_kernel<256><<<blocks, 128, 0, s>>>(p);
-  else merge_kernel<512><<<blocks, 128, 0, s>>>(p);
+  const int ppb = 256 / (p.d / 4);
+  const int blocks = (int)((pairs + ppb - 1) / ppb);
+  if (p.d == 128) merge_kernel<128><<<blocks, 256, 0, s>>>(p);
+  else if (p.d == 256) merge_kernel<256><<<blocks, 256, 0, s>>>(p);
+  else merge_kernel<512><<<blocks, 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 

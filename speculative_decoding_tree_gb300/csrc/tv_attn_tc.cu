@@ -186,7 +186,23 @@ tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ 
     }
     int j = 0, tail_uses = 0;
     bool ok = true;
+    // paged cache: lane i < 8 owns page i of a key tile; the page ids of tile
+    // t+1 are read while tile t is issued (no read waits in front of a copy)
+    const int oob_row = p.paged ? (int)(p.num_pages * p.Hkv * kPageSize) : 0;
+    auto page_row = [&](int tile) -> int {          // TMA row of this lane's page, or -1 (none)
+      if (!p.paged || tile >= npt || lane >= BN / kPageSize) return -1;
+      const int64_t pos = k_begin + (int64_t)tile * BN + lane * kPageSize;
+      if (pos >= k_end) return -1;
+      const int pid = p.page_table[(int64_t)b * p.max_pages + pos / kPageSize];
+      if (pid >= 0 && pid < p.num_pages) return (int)(((int64_t)pid * p.Hkv + g) * kPageSize);
+      set_status(p.status, TV_DEV_BAD_PAGE);
+      return oob_row;                               // out of range: the copy reads zeros
+    };
+    int row_next = page_row(0), row_k = -1, row_v = -1;
     for (int t = 0; t <= T && ok; ++t) {
+      row_v = row_k;                                // tile t-1 (for V)
+      row_k = row_next;                             // tile t   (for K)
+      row_next = page_row(t + 1);
       for (int kind = 0; kind < 2 && ok; ++kind) {           // 0: K(t), 1: V(t-1)
         const int tile = kind == 0 ? t : t - 1;
         if ((kind == 0 && t >= T) || (kind == 1 && t < 1)) continue;
@@ -200,37 +216,25 @@ tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ 
           }
           uint8_t* dst = ring + slot * CHUNK_BYTES;
           const uint32_t fb = tail_fix ? TAIL : FULL(slot);
-          if (lane == 0) {
-            if (tree) {
+          if (tree || !p.paged) {
+            if (lane == 0) {
               mbar_expect_tx(fb, CHUNK_BYTES);
-              const CUtensorMap* m = kind == 0 ? &tm_kt : &tm_vt;
-              for (int bx = 0; bx < 2; ++bx)
-                tma_load_2d(smem_u32(dst + bx * BOX_BYTES), m, fb, c * CH + bx * 64, g * p.R + o0);
-            } else if (!p.paged) {
-              mbar_expect_tx(fb, CHUNK_BYTES);
-              const CUtensorMap* m = kind == 0 ? &tm_kc : &tm_vc;
-              const int64_t row = ((int64_t)b * p.Hkv + g) * p.capacity + k_begin + (int64_t)tile * BN;
+              const CUtensorMap* m = tree ? (kind == 0 ? &tm_kt : &tm_vt) : (kind == 0 ? &tm_kc : &tm_vc);
+              const int64_t row = tree ? (int64_t)g * p.R + o0
+                                       : ((int64_t)b * p.Hkv + g) * p.capacity + k_begin + (int64_t)tile * BN;
               for (int bx = 0; bx < 2; ++bx)
                 tma_load_2d(smem_u32(dst + bx * BOX_BYTES), m, fb, c * CH + bx * 64, (int)row);
-            } else {
-              const CUtensorMap* m = kind == 0 ? &tm_kc : &tm_vc;
-              const int64_t t0 = k_begin + (int64_t)tile * BN;
-              const int valid = (int)min((int64_t)BN, k_end - t0);
-              const int npages = (valid + kPageSize - 1) / kPageSize;
-              mbar_expect_tx(fb, (uint32_t)npages * 2u * (kPageSize * 128u));
-              const int oob_row = (int)(p.num_pages * p.Hkv * kPageSize);
-              for (int pg = 0; pg < npages; ++pg) {
-                const int64_t pos = t0 + pg * kPageSize;
-                const int pid = p.page_table[(int64_t)b * p.max_pages + pos / kPageSize];
-                int row = oob_row;                       // out of range: the copy reads zeros
-                if (pid >= 0 && pid < p.num_pages) {
-                  row = (int)(((int64_t)pid * p.Hkv + g) * kPageSize);
-                } else if (c == 0) {
-                  set_status(p.status, TV_DEV_BAD_PAGE);
-                }
-                for (int bx = 0; bx < 2; ++bx)
-                  tma_load_2d(smem_u32(dst + bx * BOX_BYTES + pg * kPageSize * 128), m, fb, c * CH + bx * 64, row);
-              }
+            }
+          } else {
+            const CUtensorMap* m = kind == 0 ? &tm_kc : &tm_vc;
+            const int my_row = kind == 0 ? row_k : row_v;
+            const int npages = __popc(__ballot_sync(kAll, my_row >= 0));
+            if (lane == 0) mbar_expect_tx(fb, (uint32_t)npages * 2u * (kPageSize * 128u));
+            __syncwarp();
+            if (my_row >= 0) {
+              for (int bx = 0; bx < 2; ++bx)
+                tma_load_2d(smem_u32(dst + bx * BOX_BYTES + lane * kPageSize * 128), m, fb, c * CH + bx * 64,
+                            my_row);
             }
           }
           __syncwarp();
@@ -423,19 +427,45 @@ tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ 
       const int64_t rowg = o0 + node;
       const int h = g * G + (m0 + r) % G;
       const int64_t idx = ((int64_t)s * p.R + rowg) * p.Hq + h;
+      // a sequence with one chunk writes its normalised rows directly (the
+      // merge's arithmetic for one split); otherwise the fp32 partial
+      const bool direct = p.out != nullptr && nch == 1;
+      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
       float4* dst = reinterpret_cast<float4*>(p.o_part + idx * D + half * (D / 2));
 #pragma unroll 1
       for (int q = 0; q < D / 64; ++q) {
         uint32_t rr[32];
         tmem_ld_x32(tmem + lane_base + 256 + half * (D / 2) + q * 32, rr);
-        if (row_ok) {
+        if (row_ok && got) {
+          if (direct) {
+            const int64_t e = (rowg * p.Hq + h) * D + half * (D / 2) + q * 32;
+            if (p.out_bf16) {
+              uint4* ob = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + e);
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            dst[q * 8 + e] = make_float4(__uint_as_float(rr[4 * e]), __uint_as_float(rr[4 * e + 1]),
-                                         __uint_as_float(rr[4 * e + 2]), __uint_as_float(rr[4 * e + 3]));
+              for (int e8 = 0; e8 < 4; ++e8) {
+                uint4 u;
+                u.x = pack_bf16(__uint_as_float(rr[8 * e8 + 0]) * inv, __uint_as_float(rr[8 * e8 + 1]) * inv);
+                u.y = pack_bf16(__uint_as_float(rr[8 * e8 + 2]) * inv, __uint_as_float(rr[8 * e8 + 3]) * inv);
+                u.z = pack_bf16(__uint_as_float(rr[8 * e8 + 4]) * inv, __uint_as_float(rr[8 * e8 + 5]) * inv);
+                u.w = pack_bf16(__uint_as_float(rr[8 * e8 + 6]) * inv, __uint_as_float(rr[8 * e8 + 7]) * inv);
+                ob[e8] = u;
+              }
+            } else {
+              float4* of = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + e);
+#pragma unroll
+              for (int e4 = 0; e4 < 8; ++e4)
+                of[e4] = make_float4(__uint_as_float(rr[4 * e4]) * inv, __uint_as_float(rr[4 * e4 + 1]) * inv,
+                                     __uint_as_float(rr[4 * e4 + 2]) * inv, __uint_as_float(rr[4 * e4 + 3]) * inv);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              dst[q * 8 + e] = make_float4(__uint_as_float(rr[4 * e]), __uint_as_float(rr[4 * e + 1]),
+                                           __uint_as_float(rr[4 * e + 2]), __uint_as_float(rr[4 * e + 3]));
+          }
         }
       }
-      if (row_ok && half == 0 && got) p.ml_part[idx] = make_float2(m_ref, lsum);
+      if (row_ok && half == 0 && got && !direct) p.ml_part[idx] = make_float2(m_ref, lsum);
     }
   }
 

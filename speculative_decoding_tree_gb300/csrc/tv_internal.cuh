@@ -13,6 +13,7 @@ namespace tv {
 constexpr int kPageSize = 16;
 constexpr int kMaxNodes = 64;
 constexpr int kNumSMsDefault = 148;
+constexpr int kMaxVChunks = 32;      // vocabulary chunks per row in the argmax pass
 
 // Everything the split-KV attention kernels read, resolved on the host.
 struct AttnParams {
@@ -27,6 +28,9 @@ struct AttnParams {
   const uint64_t* anc;       // [R]
   float* o_part;             // [splits, R, Hq, d]   unnormalised partial output
   float2* ml_part;           // [splits, R, Hq]      (running max in log2 units, running sum)
+  void* out;                 // [R, Hq, d] or nullptr: a sequence with one key chunk writes its
+                             // normalised rows here instead of partials (the merge skips it)
+  int out_bf16;
   int32_t* status;
   int B, Hq, Hkv, G, d, R, max_nodes;
   int paged;
@@ -46,6 +50,7 @@ struct MergeParams {
   void* out;
   int32_t* status;
   int B, Hq, d, R, max_nodes, out_bf16;
+  int skip_single;           // rows of one-chunk sequences were written by the split pass
   int64_t max_prefix, capacity;
   int chunk, splits;
 };
