@@ -65,6 +65,7 @@ int validate(const tv_desc* d) {
 struct Plan {
   tv_plan pub;
   int G;
+  int tile_stride;
   int64_t o_part_bytes, ml_part_bytes;
 };
 
@@ -106,8 +107,14 @@ int make_plan(const tv_desc* d, Plan* p) {
   p->pub.row_tiles = row_tiles;
   p->pub.rows_per_tile = rows_per_tile;
   p->pub.grid_ctas = (int)grid;
+  // partials are tile-major: every (split, sequence, KV head, row tile) owns
+  // tile_stride rows (128 for the tensor-core kernel, whose epilogue stores
+  // whole 128-row tiles)
+  p->tile_stride = tc ? 128 : rows_per_tile;
   int64_t t;
-  if (!mul_ok(splits, d->total_rows, &t) || !mul_ok(t, d->num_q_heads, &t)) return TV_ERR_OVERFLOW;
+  if (!mul_ok(splits, d->batch, &t) || !mul_ok(t, d->num_kv_heads, &t) || !mul_ok(t, row_tiles, &t) ||
+      !mul_ok(t, p->tile_stride, &t))
+    return TV_ERR_OVERFLOW;
   int64_t o_bytes, ml_bytes;
   if (!mul_ok(t, (int64_t)d->head_dim * 4, &o_bytes) || !mul_ok(t, 8, &ml_bytes)) return TV_ERR_OVERFLOW;
   p->o_part_bytes = align_up(o_bytes, 256);
@@ -176,6 +183,7 @@ AttnParams attn_params(const tv_desc* d, const Plan& pl, const void* q, const vo
   a.scale_log2 = scale * 1.4426950408889634f;
   a.chunk = pl.pub.chunk; a.splits = pl.pub.num_splits;
   a.rows_per_tile = pl.pub.rows_per_tile; a.row_tiles = pl.pub.row_tiles;
+  a.tile_stride = pl.tile_stride;
   return a;
 }
 
@@ -196,6 +204,8 @@ int launch_merge_from(const tv_desc* d, const Plan& pl, const int32_t* plen, con
   m.out_bf16 = (d->dtype == TV_BF16 && !d->out_f32) ? 1 : 0;
   m.max_prefix = d->max_prefix; m.capacity = d->capacity;
   m.chunk = pl.pub.chunk; m.splits = pl.pub.num_splits;
+  m.Hkv = d->num_kv_heads; m.G = pl.G; m.rows_per_tile = pl.pub.rows_per_tile;
+  m.row_tiles = pl.pub.row_tiles; m.tile_stride = pl.tile_stride;
   return launch_merge(m, s) == cudaSuccess ? TV_OK : TV_ERR_CUDA;
 }
 

@@ -241,7 +241,7 @@ __global__ __launch_bounds__(128) void attn_simt_kernel(AttnParams p) {
     if (m >= nrows) continue;
     const int64_t rowg = o0 + m / p.G;
     const int h = g * p.G + m % p.G;
-    const int64_t idx = ((int64_t)s * p.R + rowg) * p.Hq + h;
+    const int64_t idx = partial_row(s, b, g, rt, m - m0, p.B, p.Hkv, p.row_tiles, p.tile_stride);
     if (direct) {
       const float inv = l_run[r] > 0.f ? 1.f / l_run[r] : 0.f;
       const int64_t obase = (rowg * p.Hq + h) * D;
@@ -296,9 +296,13 @@ __global__ __launch_bounds__(256, 2) void merge_kernel(MergeParams p) {
   const int64_t P = clamp_prefix(p.prefix_len[b], p.max_prefix, p.capacity);
   const int nch = valid ? num_chunks(P, p.chunk) : 0;
   if (p.skip_single && nch == 1) return;           // the split pass wrote this row (uniform per pair)
-  const int64_t stride = (int64_t)p.R * p.Hq;      // between splits, in (row, head) pairs
-  const float2* ml = p.ml_part + (int64_t)row * p.Hq + h;
-  const float4* op = reinterpret_cast<const float4*>(p.o_part) + ((int64_t)row * p.Hq + h) * (D / 4) + c;
+  // this (row, head) is query row m of its KV head's row tiles
+  const int m = (row - p.node_offsets[b]) * p.G + h % p.G;
+  const int rt = m / p.rows_per_tile, m_in = m - rt * p.rows_per_tile;
+  const int64_t r0 = partial_row(0, b, h / p.G, rt, m_in, p.B, p.Hkv, p.row_tiles, p.tile_stride);
+  const int64_t stride = partial_row(1, 0, 0, 0, 0, p.B, p.Hkv, p.row_tiles, p.tile_stride);   // per split
+  const float2* ml = p.ml_part + r0;
+  const float4* op = reinterpret_cast<const float4*>(p.o_part) + r0 * (D / 4) + c;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float L = 0.f, Mrun = -INFINITY;
   for (int s0 = 0; s0 < nch; s0 += 32) {

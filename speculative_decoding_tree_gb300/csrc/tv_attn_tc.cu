@@ -36,6 +36,7 @@
 // returns.
 #include <cuda.h>
 
+#include <climits>
 #include <mutex>
 
 #include "tc_ptx.cuh"
@@ -63,7 +64,7 @@ struct Cfg {
   static constexpr int NS = D == 256 ? 5 : 6;     // ring slots
   static constexpr uint32_t Q_BYTES = BM * D * 2;
   static constexpr uint32_t RING_BYTES = NS * CHUNK_BYTES;
-  static constexpr int NBARS = 2 * NS + 12;
+  static constexpr int NBARS = 2 * NS + 13;
   static constexpr uint32_t SMEM = kHeader + Q_BYTES + RING_BYTES;
   static_assert(NBARS * 8 + 8 <= 256, "barriers overflow the header");
   static_assert(SMEM <= 232448, "shared memory over the 227 KB per-block limit");
@@ -84,7 +85,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_vc,
-                  const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_vt) {
+                  const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_vt,
+                  const __grid_constant__ CUtensorMap tm_op) {
   using C = Cfg<D>;
   constexpr int CPT = C::CPT, NS = C::NS;
   constexpr unsigned kAll = 0xffffffffu;
@@ -95,13 +97,13 @@ tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ 
   const int g = blockIdx.y / p.splits;
   const int s = blockIdx.y % p.splits;
   const int b = blockIdx.z;
+  const int64_t Praw = p.prefix_len[b];            // read together with the offsets
   int o0, n;
   if (!seq_rows(p.node_offsets, b, p.R, p.max_nodes, p.status, &o0, &n)) return;
   const int G = p.G;
   const int nrows = n * G;
   const int m0 = rt * p.rows_per_tile;
   if (m0 >= nrows) return;
-  const int64_t Praw = p.prefix_len[b];
   const int64_t P = clamp_prefix(Praw, p.max_prefix, p.capacity);
   if (P != Praw && threadIdx.x == 0 && rt == 0 && s == 0 && g == 0) set_status(p.status, TV_DEV_BAD_PREFIX);
   const int nch = num_chunks(P, p.chunk);
@@ -129,7 +131,7 @@ tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ 
   auto FULL = [&](int i) { return bar(i); };
   auto EMPTY = [&](int i) { return bar(NS + i); };
   const int bq = 2 * NS;
-  const uint32_t Q_FULL = bar(bq), TAIL = bar(bq + 7), FIN = bar(bq + 8), XL = bar(bq + 11);
+  const uint32_t Q_FULL = bar(bq), TAIL = bar(bq + 7), FIN = bar(bq + 8), XL = bar(bq + 11), XST = bar(bq + 12);
   auto S_FULL = [&](int i) { return bar(bq + 1 + i); };   // QK(t) done, buffer t & 1
   auto P_FULL = [&](int i) { return bar(bq + 3 + i); };   // softmax wrote P(t), buffer t & 1
   auto O_DONE = [&](int i) { return bar(bq + 5 + i); };   // PV(t) done, alternating by t & 1
@@ -151,6 +153,7 @@ tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ 
     mbar_init(TAIL, 1);
     mbar_init(FIN, 1);
     mbar_init(XL, kSoftmax);
+    mbar_init(XST, kSoftmax);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -186,23 +189,32 @@ tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ 
     }
     int j = 0, tail_uses = 0;
     bool ok = true;
-    // paged cache: lane i < 8 owns page i of a key tile; the page ids of tile
-    // t+1 are read while tile t is issued (no read waits in front of a copy)
+    // paged cache: lane i < 8 owns page i of a key tile; page ids are read
+    // well ahead of the copies that use them
     const int oob_row = p.paged ? (int)(p.num_pages * p.Hkv * kPageSize) : 0;
-    auto page_row = [&](int tile) -> int {          // TMA row of this lane's page, or -1 (none)
-      if (!p.paged || tile >= npt || lane >= BN / kPageSize) return -1;
+    auto page_id = [&](int tile) -> int {           // raw page id of this lane's page, or INT_MIN (none)
+      if (!p.paged || tile >= npt || lane >= BN / kPageSize) return INT_MIN;
       const int64_t pos = k_begin + (int64_t)tile * BN + lane * kPageSize;
-      if (pos >= k_end) return -1;
-      const int pid = p.page_table[(int64_t)b * p.max_pages + pos / kPageSize];
+      if (pos >= k_end) return INT_MIN;
+      return p.page_table[(int64_t)b * p.max_pages + pos / kPageSize];
+    };
+    auto page_row = [&](int pid) -> int {           // TMA row of a page id, checked where it is used
+      if (pid == INT_MIN) return -1;
       if (pid >= 0 && pid < p.num_pages) return (int)(((int64_t)pid * p.Hkv + g) * kPageSize);
       set_status(p.status, TV_DEV_BAD_PAGE);
       return oob_row;                               // out of range: the copy reads zeros
     };
-    int row_next = page_row(0), row_k = -1, row_v = -1;
+    // page ids four tiles ahead (a read takes about a microsecond; nothing
+    // branches on a value until it is used)
+    int pid_a = page_id(0), pid_b = page_id(1), pid_c = page_id(2), pid_d = page_id(3);
+    int row_k = -1, row_v = -1;
     for (int t = 0; t <= T && ok; ++t) {
       row_v = row_k;                                // tile t-1 (for V)
-      row_k = row_next;                             // tile t   (for K)
-      row_next = page_row(t + 1);
+      row_k = page_row(pid_a);                      // tile t   (for K)
+      pid_a = pid_b;
+      pid_b = pid_c;
+      pid_c = pid_d;
+      pid_d = page_id(t + 4);
       for (int kind = 0; kind < 2 && ok; ++kind) {           // 0: K(t), 1: V(t-1)
         const int tile = kind == 0 ? t : t - 1;
         if ((kind == 0 && t >= T) || (kind == 1 && t < 1)) continue;
@@ -415,8 +427,15 @@ tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ 
       mbar_arrive(P_FULL(t & 1));
     }
     // epilogue: the last P V has landed (its commit covers every earlier
-    // MMA); add the two halves' sums; write this chunk's partial
+    // MMA); add the two halves' sums.  A sequence with one chunk writes its
+    // normalised rows directly (the merge's arithmetic for one split).
+    // Otherwise the fp32 tile goes through shared memory (the ring, idle
+    // now; 128-byte swizzled 32-column boxes) and out with TMA stores into
+    // this CTA's own tile of the partials.
     const int u = T - 1;
+    const bool direct = p.out != nullptr && nch == 1;
+    const int64_t tile = partial_row(s, b, g, rt, 0, p.B, p.Hkv, p.row_tiles, BM) / BM;
+    bool staged = false;
     if (ok && __all_sync(kAll, mbar_wait(O_DONE(u & 1), (u >> 1) & 1, abort_flag, kWaitNs))) {
       tc_fence_after();
       float* xb = xch + (T & 1) * 256;
@@ -426,47 +445,60 @@ tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ 
       const float lsum = l + xb[(half ^ 1) * 128 + r];
       const int64_t rowg = o0 + node;
       const int h = g * G + (m0 + r) % G;
-      const int64_t idx = ((int64_t)s * p.R + rowg) * p.Hq + h;
-      // a sequence with one chunk writes its normalised rows directly (the
-      // merge's arithmetic for one split); otherwise the fp32 partial
-      const bool direct = p.out != nullptr && nch == 1;
       const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-      float4* dst = reinterpret_cast<float4*>(p.o_part + idx * D + half * (D / 2));
 #pragma unroll 1
       for (int q = 0; q < D / 64; ++q) {
         uint32_t rr[32];
         tmem_ld_x32(tmem + lane_base + 256 + half * (D / 2) + q * 32, rr);
-        if (row_ok && got) {
-          if (direct) {
-            const int64_t e = (rowg * p.Hq + h) * D + half * (D / 2) + q * 32;
-            if (p.out_bf16) {
-              uint4* ob = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + e);
+        if (!got) continue;
+        if (direct) {
+          if (!row_ok) continue;
+          const int64_t e = (rowg * p.Hq + h) * D + half * (D / 2) + q * 32;
+          if (p.out_bf16) {
+            uint4* ob = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + e);
 #pragma unroll
-              for (int e8 = 0; e8 < 4; ++e8) {
-                uint4 u;
-                u.x = pack_bf16(__uint_as_float(rr[8 * e8 + 0]) * inv, __uint_as_float(rr[8 * e8 + 1]) * inv);
-                u.y = pack_bf16(__uint_as_float(rr[8 * e8 + 2]) * inv, __uint_as_float(rr[8 * e8 + 3]) * inv);
-                u.z = pack_bf16(__uint_as_float(rr[8 * e8 + 4]) * inv, __uint_as_float(rr[8 * e8 + 5]) * inv);
-                u.w = pack_bf16(__uint_as_float(rr[8 * e8 + 6]) * inv, __uint_as_float(rr[8 * e8 + 7]) * inv);
-                ob[e8] = u;
-              }
-            } else {
-              float4* of = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + e);
-#pragma unroll
-              for (int e4 = 0; e4 < 8; ++e4)
-                of[e4] = make_float4(__uint_as_float(rr[4 * e4]) * inv, __uint_as_float(rr[4 * e4 + 1]) * inv,
-                                     __uint_as_float(rr[4 * e4 + 2]) * inv, __uint_as_float(rr[4 * e4 + 3]) * inv);
+            for (int e8 = 0; e8 < 4; ++e8) {
+              uint4 w4;
+              w4.x = pack_bf16(__uint_as_float(rr[8 * e8 + 0]) * inv, __uint_as_float(rr[8 * e8 + 1]) * inv);
+              w4.y = pack_bf16(__uint_as_float(rr[8 * e8 + 2]) * inv, __uint_as_float(rr[8 * e8 + 3]) * inv);
+              w4.z = pack_bf16(__uint_as_float(rr[8 * e8 + 4]) * inv, __uint_as_float(rr[8 * e8 + 5]) * inv);
+              w4.w = pack_bf16(__uint_as_float(rr[8 * e8 + 6]) * inv, __uint_as_float(rr[8 * e8 + 7]) * inv);
+              ob[e8] = w4;
             }
           } else {
+            float4* of = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + e);
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              dst[q * 8 + e] = make_float4(__uint_as_float(rr[4 * e]), __uint_as_float(rr[4 * e + 1]),
-                                           __uint_as_float(rr[4 * e + 2]), __uint_as_float(rr[4 * e + 3]));
+            for (int e4 = 0; e4 < 8; ++e4)
+              of[e4] = make_float4(__uint_as_float(rr[4 * e4]) * inv, __uint_as_float(rr[4 * e4 + 1]) * inv,
+                                   __uint_as_float(rr[4 * e4 + 2]) * inv, __uint_as_float(rr[4 * e4 + 3]) * inv);
           }
+        } else {
+          // box (half * D/64 + q): 128 rows x 128 bytes, 16-byte chunk c of
+          // row r at chunk c ^ (r & 7)
+          uint8_t* box = ring + (uint32_t)(half * (D / 64) + q) * (BM * 128) + r * 128;
+#pragma unroll
+          for (int c4 = 0; c4 < 8; ++c4)
+            *reinterpret_cast<uint4*>(box + ((c4 ^ (r & 7)) * 16)) =
+                make_uint4(rr[4 * c4], rr[4 * c4 + 1], rr[4 * c4 + 2], rr[4 * c4 + 3]);
         }
       }
-      if (row_ok && half == 0 && got && !direct) p.ml_part[idx] = make_float2(m_ref, lsum);
+      if (!direct && got) {
+        p.ml_part[tile * BM + r] = make_float2(row_ok ? m_ref : -INFINITY, row_ok ? lsum : 0.f);
+        staged = true;
+      }
     }
+    // every softmax thread arrives (staged or not); one issues the stores
+    fence_proxy_async_smem();
+    mbar_arrive(XST);
+    if (tid == 128) {
+      const bool all_in = mbar_wait(XST, 0, abort_flag, kWaitNs);
+      if (all_in && !direct && !*abort_flag) {
+        for (int bx = 0; bx < D / 32; ++bx) tma_store_2d(&tm_op, smem_u32(ring + bx * (BM * 128)), bx * 32, (int)(tile * BM));
+        bulk_commit_group();
+        bulk_wait_all();
+      }
+    }
+    (void)staged;
   }
 
   // ---------------------------------------------------------------- teardown
@@ -502,11 +534,11 @@ EncodeTiledFn encode_fn() {
 }
 
 bool encode(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
-            const cuuint32_t* box) {
+            const cuuint32_t* box, CUtensorMapDataType type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, box, es,
+  return fn(m, type, rank, const_cast<void*>(ptr), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -537,6 +569,15 @@ cudaError_t launch_tc_t(const AttnParams& p, cudaStream_t st) {
     if (!encode(&mkt, p.k_tree, 2, dims, strides, box) || !encode(&mvt, p.v_tree, 2, dims, strides, box))
       return cudaErrorInvalidValue;
   }
+  CUtensorMap mop;
+  {
+    // partials: [tiles * 128 rows, D] fp32, stored as 32-column boxes
+    const cuuint64_t tiles = (cuuint64_t)p.splits * p.B * p.Hkv * p.row_tiles;
+    cuuint64_t dims[2] = {(cuuint64_t)D, tiles * BM};
+    cuuint64_t strides[1] = {(cuuint64_t)D * 4};
+    cuuint32_t box[2] = {32, BM};
+    if (!encode(&mop, p.o_part, 2, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32)) return cudaErrorInvalidValue;
+  }
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(tv_attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -545,7 +586,7 @@ cudaError_t launch_tc_t(const AttnParams& p, cudaStream_t st) {
     configured = true;
   }
   dim3 grid(p.row_tiles, p.Hkv * p.splits, p.B);
-  tv_attn_tc_kernel<D><<<grid, kThreads, Cfg<D>::SMEM, st>>>(p, mq, mkc, mvc, mkt, mvt);
+  tv_attn_tc_kernel<D><<<grid, kThreads, Cfg<D>::SMEM, st>>>(p, mq, mkc, mvc, mkt, mvt, mop);
   return cudaGetLastError();
 }
 

@@ -6,7 +6,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
-#include "../../include/tree_verify.h"
+#include "tree_verify.h"
 
 namespace tv {
 
@@ -26,8 +26,9 @@ struct AttnParams {
   const void* k_tree;        // [Hkv, R, d]
   const void* v_tree;
   const uint64_t* anc;       // [R]
-  float* o_part;             // [splits, R, Hq, d]   unnormalised partial output
-  float2* ml_part;           // [splits, R, Hq]      (running max in log2 units, running sum)
+  float* o_part;             // [tiles, tile_stride, d]  unnormalised partial output, tile-major:
+                             // tile = ((split * B + b) * Hkv + g) * row_tiles + row_tile
+  float2* ml_part;           // [tiles, tile_stride]     (running max in log2 units, running sum)
   void* out;                 // [R, Hq, d] or nullptr: a sequence with one key chunk writes its
                              // normalised rows here instead of partials (the merge skips it)
   int out_bf16;
@@ -40,7 +41,14 @@ struct AttnParams {
   int splits;                // splits in the grid (covers max_prefix)
   int rows_per_tile;         // query rows per row tile (node x group head)
   int row_tiles;
+  int tile_stride;           // partial rows reserved per tile (>= rows_per_tile)
 };
+
+// Partial-row index of query row m_in of row tile rt of (split, b, g).
+__host__ __device__ inline int64_t partial_row(int split, int b, int g, int rt, int m_in, int B, int Hkv,
+                                               int row_tiles, int tile_stride) {
+  return ((((int64_t)split * B + b) * Hkv + g) * row_tiles + rt) * tile_stride + m_in;
+}
 
 struct MergeParams {
   const int32_t* prefix_len;
@@ -51,6 +59,7 @@ struct MergeParams {
   int32_t* status;
   int B, Hq, d, R, max_nodes, out_bf16;
   int skip_single;           // rows of one-chunk sequences were written by the split pass
+  int Hkv, G, rows_per_tile, row_tiles, tile_stride;
   int64_t max_prefix, capacity;
   int chunk, splits;
 };
