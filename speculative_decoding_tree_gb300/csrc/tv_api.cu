@@ -81,7 +81,10 @@ int make_plan(const tv_desc* d, Plan* p) {
     rows_per_tile = 4 * rpw;
   }
   int row_tiles = (d->max_nodes * G + rows_per_tile - 1) / rows_per_tile;
-  int64_t units = (int64_t)d->batch * d->num_kv_heads * row_tiles;
+  // two or more 128-row tiles per KV head: CTA pairs (cta_group::2) share each K/V tile
+  const bool pairs = tc && row_tiles >= 2;
+  const int launched_tiles = pairs ? 2 * ((row_tiles + 1) / 2) : row_tiles;
+  int64_t units = (int64_t)d->batch * d->num_kv_heads * launched_tiles;
   int64_t sms = num_sms();
   int64_t L = d->max_prefix;
   int64_t chunk;
@@ -101,7 +104,7 @@ int make_plan(const tv_desc* d, Plan* p) {
   int64_t grid = units * splits;
   if (grid > ((int64_t)1 << 31) - 1) return TV_ERR_OVERFLOW;
   p->G = G;
-  p->pub.kernel = tc ? 1 : 0;
+  p->pub.kernel = pairs ? 2 : (tc ? 1 : 0);
   p->pub.num_splits = splits;
   p->pub.chunk = (int)chunk;
   p->pub.row_tiles = row_tiles;
@@ -188,7 +191,9 @@ AttnParams attn_params(const tv_desc* d, const Plan& pl, const void* q, const vo
 }
 
 int launch_partials(const tv_desc* d, const Plan& pl, const AttnParams& a, cudaStream_t s) {
-  cudaError_t e = pl.pub.kernel == 1 ? launch_attn_tc(a, s) : launch_attn_simt(a, d->dtype, s);
+  cudaError_t e = pl.pub.kernel == 2   ? launch_attn_tc2(a, s)
+                  : pl.pub.kernel == 1 ? launch_attn_tc(a, s)
+                                       : launch_attn_simt(a, d->dtype, s);
   return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
 }
 

@@ -55,7 +55,8 @@ constexpr uint32_t CHUNK_BYTES = 2 * BOX_BYTES; // 128 keys x 128 columns
 constexpr uint64_t kWaitNs = 1000000000ull;
 constexpr float kRescaleThreshold = 8.0f;       // rescale O when the max grows by > 2^8
 constexpr int kThreads = 384;                   // warps 0 producer, 1 MMA, 2-3 idle, 4-11 softmax
-constexpr int kSoftmax = 256;                   // two warpgroups, each half of a row's keys
+constexpr int kSoftmax = 256;
+constexpr int kSoftmaxWarps = kSoftmax / 32;   // barriers count warps: lane 0 arrives after __syncwarp                   // two warpgroups, each half of a row's keys
 constexpr uint32_t kHeader = 3072;              // barriers, TMEM address, row exchange (then 1 KB aligned)
 
 template <int D>
@@ -146,14 +147,14 @@ tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ 
     mbar_init(Q_FULL, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(S_FULL(i), 1);
-      mbar_init(P_FULL(i), kSoftmax);
+      mbar_init(P_FULL(i), kSoftmaxWarps);         // one arrive per softmax warp
       mbar_init(O_DONE(i), 1);
-      mbar_init(XCH(i), kSoftmax);
+      mbar_init(XCH(i), kSoftmaxWarps);
     }
     mbar_init(TAIL, 1);
     mbar_init(FIN, 1);
-    mbar_init(XL, kSoftmax);
-    mbar_init(XST, kSoftmax);
+    mbar_init(XL, kSoftmaxWarps);
+    mbar_init(XST, kSoftmaxWarps);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -380,7 +381,8 @@ tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ 
       // exchange the half-row maximum with the other half
       float* xb = xch + (t & 1) * 256;
       xb[half * 128 + r] = mx;
-      mbar_arrive(XCH(t & 1));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(XCH(t & 1));
       if (!__all_sync(kAll, mbar_wait(XCH(t & 1), (t >> 1) & 1, abort_flag, kWaitNs))) { ok = false; break; }
       mx = fmaxf(mx, xb[(half ^ 1) * 128 + r]);
       const float m_tile = mx == -INFINITY ? -INFINITY : mx * c2;
@@ -424,7 +426,8 @@ tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ 
       l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
       tmem_st_x32(sbuf + half * 32, pk);                   // P over the S columns, bf16 pairs
       tc_fence_before();
-      mbar_arrive(P_FULL(t & 1));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(P_FULL(t & 1));
     }
     // epilogue: the last P V has landed (its commit covers every earlier
     // MMA); add the two halves' sums.  A sequence with one chunk writes its
@@ -440,7 +443,8 @@ tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ 
       tc_fence_after();
       float* xb = xch + (T & 1) * 256;
       xb[half * 128 + r] = l;
-      mbar_arrive(XL);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(XL);
       const bool got = __all_sync(kAll, mbar_wait(XL, 0, abort_flag, kWaitNs));
       const float lsum = l + xb[(half ^ 1) * 128 + r];
       const int64_t rowg = o0 + node;
@@ -489,7 +493,8 @@ tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ 
     }
     // every softmax thread arrives (staged or not); one issues the stores
     fence_proxy_async_smem();
-    mbar_arrive(XST);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(XST);
     if (tid == 128) {
       const bool all_in = mbar_wait(XST, 0, abort_flag, kWaitNs);
       if (all_in && !direct && !*abort_flag) {

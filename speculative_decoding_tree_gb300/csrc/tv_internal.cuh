@@ -100,6 +100,7 @@ __device__ inline bool seq_rows(const int32_t* offs, int b, int R, int max_nodes
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_attn_simt(const AttnParams& p, int dtype, cudaStream_t s);
 cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t s);
+cudaError_t launch_attn_tc2(const AttnParams& p, cudaStream_t s);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);
 cudaError_t launch_tree_mask(const int32_t* parents, const int32_t* offs, uint64_t* anc, int32_t* depth,
                              int32_t* status, int B, int R, int max_nodes, cudaStream_t s);

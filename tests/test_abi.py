@@ -97,10 +97,11 @@ def test_workspace_and_plan(L):
     plan = tv.tv_attn_plan(d)
     assert plan["num_splits"] >= 1 and plan["chunk"] * plan["num_splits"] >= 4096
     assert plan["rows_per_tile"] * plan["row_tiles"] >= 64 * 4
-    assert plan["kernel"] == 1                       # bf16, d256, 256 rows per KV head: tensor cores
+    assert plan["kernel"] == 2                       # bf16, d256, 256 rows per KV head: CTA pairs
     assert plan["rows_per_tile"] == 128 and plan["chunk"] % 128 == 0
+    assert tv.tv_attn_plan(_desc(max_nodes=16, total_rows=16))["kernel"] == 1   # 64 rows: one CTA per tile
     assert tv.tv_attn_plan(_desc(dtype=tv.F32))["kernel"] == 0
     assert tv.tv_attn_plan(_desc(head_dim=512))["kernel"] == 0
     assert tv.tv_attn_plan(_desc(max_nodes=2, total_rows=2))["kernel"] == 0   # 8 rows per KV head
     g3 = tv.tv_attn_plan(_desc(num_q_heads=24))                               # G = 3: 126-row tiles
-    assert g3["kernel"] == 1 and g3["rows_per_tile"] == 126
+    assert g3["kernel"] == 2 and g3["rows_per_tile"] == 126

@@ -155,16 +155,16 @@ def test_accept_commit_chain_of_steps():
     check_step(w2, st2, ref2)
 
 
-@pytest.mark.parametrize("d", [128, 256])
-def test_growing_scores_force_rescale(d):
+@pytest.mark.parametrize("d,nodes,kernel", [(128, 20, 1), (256, 20, 1), (128, 40, 2), (256, 40, 2)])
+def test_growing_scores_force_rescale(d, nodes, kernel):
     # prefix keys whose scores grow along the prefix: the running maximum
-    # climbs tile after tile, so the tensor-core kernel must rescale O
-    spec = wl.CONFIGS[3].replace(prefix=(1500, 1500), vocab=64, d=d, hq=8, hkv=2, tree="random:20,20,6",
+    # climbs tile after tile, so the tensor-core kernels must rescale O
+    spec = wl.CONFIGS[3].replace(prefix=(1500, 1500), vocab=64, d=d, hq=8, hkv=2, tree=f"random:{nodes},{nodes},6",
                                  seed=4242 + d)
     w = workload(spec)
     P = 1500
     ramp = (1.0 + 0.02 * torch.arange(P, dtype=torch.float32)).view(1, 1, P, 1)
     w.k_cache[:, :, :P] = (w.k_cache[:, :, :P].float() * ramp).to(torch.bfloat16)
     st = run(w)
-    assert tv.tv_attn_plan(st.desc)["kernel"] == 1
+    assert tv.tv_attn_plan(st.desc)["kernel"] == kernel
     check_step(w, st, oracle.verify_step(w))
