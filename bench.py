@@ -272,65 +272,69 @@ def run_ours(args, ws, rank):
     torch.cuda.synchronize()
     elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), ws)
 
-    # per-kernel durations: each input set's step captured once more with
-    # timing events between the calls (external event-record nodes), the
-    # graphs replayed back to back and the events read after each round
-    names = ("mask", "attn_split", "attn_merge", "accept_commit")
-    samples = {k: [] for k in names}
-    timing_mode = "events inside CUDA-graph replays"
-    try:
-        evsets = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)] for _ in sets]
-        tgraphs = []
-        for st_, e in zip(sets, evsets):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=cap_stream):
-                st_.prefix_len.copy_(st_.p0, non_blocking=True)
-                e[0].record()
-                st_.mask()
-                e[1].record()
-                st_.partials()
-                e[2].record()
-                st_.merge()
-                e[3].record()
-                st_.accept_commit()
-                e[4].record()
-            tgraphs.append(g)
-        rounds = max(1, min(args.steps, 200) // nsets)
-        for _ in range(rounds):
+    # per-kernel durations: K back-to-back launches of one call in one CUDA
+    # graph, rotating over the input sets, bracketed by two events; the
+    # per-launch time is the total over K (gaps between launches included).
+    # Every split launch reads more than L2 holds since its set was last read.
+    def b2b_us(calls, reps=5):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap_stream):
+            for c in calls:
+                c()
+        g.replay()
+        torch.cuda.synchronize()
+        out = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             torch.cuda._sleep(2_000_000)
-            for g in tgraphs:
-                g.replay()
+            e0.record()
+            g.replay()
+            e1.record()
             torch.cuda.synchronize()
-            for e in evsets:
-                for k, name in enumerate(names):
-                    samples[name].append(e[k].elapsed_time(e[k + 1]))
-    except (TypeError, RuntimeError):
-        # no external events in this torch: eager calls with events between
-        timing_mode = "events between eager calls"
-        n_k = min(args.steps, 200)
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n_k)]
-        torch.cuda.synchronize()
-        torch.cuda._sleep(80_000_000)
-        for i in range(n_k):
-            st_ = sets[i % nsets]
-            e = evs[i]
+            out.append(e0.elapsed_time(e1) * 1e3 / len(calls))
+        return statistics.median(out)
+
+    for st_ in sets:                                  # the timed steps advanced prefix_len
+        st_.prefix_len.copy_(st_.p0)
+    torch.cuda.synchronize()
+    n_b2b = max(24, 8 * nsets)
+    pick = [sets[i % nsets] for i in range(n_b2b)]
+    split_us = b2b_us([st_.partials for st_ in pick])
+    attn_us = b2b_us([st_.attn for st_ in pick])      # the whole tree_verify_attn call
+    mask_us = b2b_us([st_.mask for st_ in pick])
+    merge_us = b2b_us([st_.merge for st_ in pick])
+
+    # accept + commit: the commit advances prefix_len, so each call starts
+    # from its set's original prefix (a copy node before each call); the
+    # logits rotate over enough copies that they come from HBM each time
+    # (each set keeps logits of its own shape: sets differ in their row count)
+    own = [st_.logits for st_ in sets]
+    pool = [(st_, st_.logits) for st_ in sets]
+    pool_bytes = sum(t.numel() * t.element_size() for t in own)
+    while pool_bytes < 3 * L2_BYTES:
+        st_ = sets[len(pool) % nsets]
+        pool.append((st_, st_.logits.clone()))
+        pool_bytes += st_.logits.numel() * st_.logits.element_size()
+    acc_calls = []
+    for i in range(max(len(pool), n_b2b)):
+        st_, lg = pool[i % len(pool)]
+
+        def call(st_=st_, lg=lg):
             st_.prefix_len.copy_(st_.p0, non_blocking=True)
-            e[0].record()
-            st_.mask()
-            e[1].record()
-            st_.partials()
-            e[2].record()
-            st_.merge()
-            e[3].record()
+            st_.logits = lg
             st_.accept_commit()
-            e[4].record()
-        torch.cuda.synchronize()
-        for e in evs:
-            for k, name in enumerate(names):
-                samples[name].append(e[k].elapsed_time(e[k + 1]))
+        acc_calls.append(call)
+    acc_us = b2b_us(acc_calls)
+    for st_, lg in zip(sets, own):
+        st_.logits = lg
+        st_.prefix_len.copy_(st_.p0)
+    del pool
+    timing_mode = ("back-to-back launches of each call in one CUDA graph over the rotating input sets, "
+                   "programmatic dependent launch between them; per launch = events around the graph / launches")
     clocks = sampler.stop() if sampler else None
-    mask_us, split_us, merge_us, acc_us = (statistics.mean(samples[k]) * 1e3 for k in names)
-    status = sum(int(st.status[0].item()) for st in sets)
+    status = 0
+    for st_ in sets:
+        status |= int(st_.status[0].item())
 
     # e2e through the public API with host buffers: per step copy the step's
     # inputs in from pinned memory, run the step, copy the results out
@@ -380,7 +384,7 @@ def run_ours(args, ws, rank):
             "kernel_timing": timing_mode,
         },
         "roofline": {
-            "kernel": "tv_attn_tc_kernel" if plan["kernel"] == 1 else "attn_simt_kernel",
+            "kernel": {0: "attn_simt_kernel", 1: "tv_attn_tc_kernel", 2: "tv_attn_tc2_kernel"}[plan["kernel"]],
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "peak_source": peak_kind,
             "traffic": profiled_traffic(spec.name),
@@ -388,12 +392,12 @@ def run_ours(args, ws, rank):
         },
         "e2e": {"value": round(ws * rows * n_e2e / (e2e_ms / 1e3), 1), "unit": "rows/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": st.KERNELS_PER_STEP * args.steps,
+        "gpu_launches": st.kernels_per_step() * args.steps,
         "clocks": clocks,
         "breakdown_us": {"mask": round(mask_us, 2), "attn_split": round(split_us, 2),
                          "attn_merge": round(merge_us, 2), "accept_commit": round(acc_us, 2)},
-        "attn_call": {"gbs": round(ab["attn"] / ((split_us + merge_us) * 1e-6) / 1e9, 1),
-                      "frac": round(ab["attn"] / ((split_us + merge_us) * 1e-6) / 1e9 / peak, 4),
+        "attn_call": {"us": round(attn_us, 2), "gbs": round(ab["attn"] / (attn_us * 1e-6) / 1e9, 1),
+                      "frac": round(ab["attn"] / (attn_us * 1e-6) / 1e9 / peak, 4),
                       "algorithmic_bytes": ab["attn"]},
         "accept_commit_us": round(acc_us, 2),
         "plan": plan,

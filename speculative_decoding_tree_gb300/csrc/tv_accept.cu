@@ -24,6 +24,8 @@ __global__ void tree_mask_kernel(const int32_t* __restrict__ parents, const int3
                                  uint64_t* __restrict__ anc, int32_t* __restrict__ depth, int32_t* status,
                                  int B, int R, int max_nodes) {
   __shared__ int s_par[kMaxNodes];
+  dep_wait();
+  dep_launch();
   const int b = blockIdx.x;
   if (b == B - 1 && threadIdx.x == 0 && offs[B] != R) set_status(status, TV_DEV_BAD_OFFSETS);
   int o0, n;
@@ -134,6 +136,8 @@ __global__ __launch_bounds__(256) void argmax_partial_kernel(const void* __restr
   constexpr int ES = BF16 ? 2 : 4;
   constexpr int PER = 16 / ES;                       // elements per 16-byte load
   constexpr int UNROLL = 4;
+  dep_wait();
+  dep_launch();
   const int row = blockIdx.y, c = blockIdx.x;
   const int v0 = c * vlen;
   const int v1 = min(V, v0 + vlen);
@@ -207,6 +211,8 @@ __global__ __launch_bounds__(256) void walk_commit_kernel(AcceptParams p) {
   __shared__ int s_pi[kMaxNodes * kMaxVChunks];
   __shared__ int s_P, s_k, s_ok;
 
+  dep_wait();
+  dep_launch();
   const int b = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int o0, n;
@@ -394,20 +400,16 @@ __global__ __launch_bounds__(256) void walk_commit_kernel(AcceptParams p) {
 
 cudaError_t launch_tree_mask(const int32_t* parents, const int32_t* offs, uint64_t* anc, int32_t* depth,
                              int32_t* status, int B, int R, int max_nodes, cudaStream_t s) {
-  tree_mask_kernel<<<B, kMaxNodes, 0, s>>>(parents, offs, anc, depth, status, B, R, max_nodes);
-  return cudaGetLastError();
+  return launch_dep(tree_mask_kernel, dim3(B), dim3(kMaxNodes), 0, s, parents, offs, anc, depth, status, B, R,
+                    max_nodes);
 }
 
 cudaError_t launch_accept_commit(const AcceptParams& p, cudaStream_t s) {
   dim3 grid(p.vchunks, p.R);
-  if (p.logits_bf16)
-    argmax_partial_kernel<true><<<grid, 256, 0, s>>>(p.logits, p.V, p.vchunk_len, p.vchunks, p.am_val, p.am_idx);
-  else
-    argmax_partial_kernel<false><<<grid, 256, 0, s>>>(p.logits, p.V, p.vchunk_len, p.vchunks, p.am_val, p.am_idx);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_dep(p.logits_bf16 ? argmax_partial_kernel<true> : argmax_partial_kernel<false>, grid,
+                             dim3(256), 0, s, p.logits, p.V, p.vchunk_len, p.vchunks, p.am_val, p.am_idx);
   if (e != cudaSuccess) return e;
-  walk_commit_kernel<<<p.B, 256, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_dep(walk_commit_kernel, dim3(p.B), dim3(256), 0, s, p);
 }
 
 }  // namespace tv

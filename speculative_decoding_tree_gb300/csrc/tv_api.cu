@@ -65,6 +65,7 @@ int validate(const tv_desc* d) {
 struct Plan {
   tv_plan pub;
   int G;
+  int tree_tile;             // num_chunks rule: 0, or the key tile (one-wave plans)
   int tile_stride;
   int64_t o_part_bytes, ml_part_bytes;
 };
@@ -88,22 +89,31 @@ int make_plan(const tv_desc* d, Plan* p) {
   int64_t sms = num_sms();
   int64_t L = d->max_prefix;
   int64_t chunk;
+  int tree_tile = 0;
   if (d->batch == 1) {
-    // one wave: the prefix split evenly over the SMs
+    // one wave: at most sms / units splits; the fewest key tiles per chunk
+    // with which the prefix, and the tree in the last chunk or on its own
+    // (num_chunks), fit that many splits
     int64_t want = sms / units;
     if (want < 1) want = 1;
-    chunk = (L + want - 1) / want;
+    const int64_t tiles = (L + key_tile - 1) / key_tile;
+    if (tiles > ((int64_t)1 << 30) / key_tile) return TV_ERR_OVERFLOW;
+    tree_tile = key_tile;
+    int64_t c = (tiles + want - 1) / want;
+    if (c < 1) c = 1;
+    while (c <= tiles && num_chunks(L, (int)(c * key_tile), tree_tile) > want) ++c;
+    chunk = c * key_tile;
   } else {
     // ragged batch: fixed 1024-key chunks (about 8 key tiles) so that the
     // block scheduler balances sequences of different lengths
-    chunk = 1024;
+    chunk = align_up(1024, key_tile);
   }
-  chunk = align_up(chunk < 1 ? 1 : chunk, key_tile);
   if (chunk > (int64_t)1 << 30) return TV_ERR_OVERFLOW;
-  int splits = num_chunks(L, (int)chunk);
+  int splits = num_chunks(L, (int)chunk, tree_tile);
   int64_t grid = units * splits;
   if (grid > ((int64_t)1 << 31) - 1) return TV_ERR_OVERFLOW;
   p->G = G;
+  p->tree_tile = tree_tile;
   p->pub.kernel = pairs ? 2 : (tc ? 1 : 0);
   p->pub.num_splits = splits;
   p->pub.chunk = (int)chunk;
@@ -164,6 +174,13 @@ int check_attn_ptrs(const tv_desc* d, const void* q, const void* kc, const void*
   return TV_OK;
 }
 
+// Partials are stored in bf16 by the tensor-core kernels when the output is
+// bf16: they are normalised (O_s / l_s), and P already enters the PV product
+// rounded to bf16, so they carry no more rounding than the output itself.
+int part_bf16(const tv_desc* d, const Plan& pl) {
+  return (pl.pub.kernel != 0 && d->dtype == TV_BF16 && !d->out_f32) ? 1 : 0;
+}
+
 AttnParams attn_params(const tv_desc* d, const Plan& pl, const void* q, const void* kc, const void* vc,
                        const int32_t* pt, const int32_t* plen, const int32_t* no, const void* kt,
                        const void* vt, const uint64_t* anc, void* ws, int32_t* st) {
@@ -184,9 +201,10 @@ AttnParams attn_params(const tv_desc* d, const Plan& pl, const void* q, const vo
   a.max_prefix = d->max_prefix;
   float scale = d->scale > 0.f ? d->scale : 1.0f / std::sqrt((float)d->head_dim);
   a.scale_log2 = scale * 1.4426950408889634f;
-  a.chunk = pl.pub.chunk; a.splits = pl.pub.num_splits;
+  a.chunk = pl.pub.chunk; a.tree_tile = pl.tree_tile; a.splits = pl.pub.num_splits;
   a.rows_per_tile = pl.pub.rows_per_tile; a.row_tiles = pl.pub.row_tiles;
   a.tile_stride = pl.tile_stride;
+  a.part_bf16 = part_bf16(d, pl);
   return a;
 }
 
@@ -205,12 +223,15 @@ int launch_merge_from(const tv_desc* d, const Plan& pl, const int32_t* plen, con
   m.o_part = reinterpret_cast<const float*>(ws);
   m.ml_part = reinterpret_cast<const float2*>(reinterpret_cast<const char*>(ws) + pl.o_part_bytes);
   m.out = out; m.status = st;
+  m.part_bf16 = part_bf16(d, pl);
   m.B = d->batch; m.Hq = d->num_q_heads; m.d = d->head_dim; m.R = d->total_rows; m.max_nodes = d->max_nodes;
   m.out_bf16 = (d->dtype == TV_BF16 && !d->out_f32) ? 1 : 0;
   m.max_prefix = d->max_prefix; m.capacity = d->capacity;
-  m.chunk = pl.pub.chunk; m.splits = pl.pub.num_splits;
+  m.chunk = pl.pub.chunk; m.tree_tile = pl.tree_tile; m.splits = pl.pub.num_splits;
   m.Hkv = d->num_kv_heads; m.G = pl.G; m.rows_per_tile = pl.pub.rows_per_tile;
   m.row_tiles = pl.pub.row_tiles; m.tile_stride = pl.tile_stride;
+  merge_shape(d->batch * d->num_kv_heads * pl.pub.row_tiles, pl.tile_stride, d->head_dim, m.part_bf16 ? 2 : 4,
+              pl.pub.num_splits, num_sms(), &m.slab_rows, &m.batch_splits);
   return launch_merge(m, s) == cudaSuccess ? TV_OK : TV_ERR_CUDA;
 }
 

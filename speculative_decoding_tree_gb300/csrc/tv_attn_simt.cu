@@ -57,6 +57,8 @@ __global__ __launch_bounds__(128) void attn_simt_kernel(AttnParams p) {
   float* vs = ks + kKeyTile * KS;                         // [32][D]
   float* ps = vs + kKeyTile * D;                          // [4 warps][RPW][32]
   __shared__ uint64_t s_anc[ROWS];
+  dep_wait();
+  dep_launch();
 
   const int b = blockIdx.z;
   const int s = blockIdx.y;
@@ -70,7 +72,7 @@ __global__ __launch_bounds__(128) void attn_simt_kernel(AttnParams p) {
   const int64_t Praw = p.prefix_len[b];
   const int64_t P = clamp_prefix(Praw, p.max_prefix, p.capacity);
   if (P != Praw && threadIdx.x == 0 && rt == 0 && s == 0 && g == 0) set_status(p.status, TV_DEV_BAD_PREFIX);
-  const int nch = num_chunks(P, p.chunk);
+  const int nch = num_chunks(P, p.chunk, p.tree_tile);
   if (s >= nch) return;
   const int64_t k_begin = (int64_t)s * p.chunk;
   const int64_t k_end = min(P, k_begin + p.chunk);
@@ -241,7 +243,7 @@ __global__ __launch_bounds__(128) void attn_simt_kernel(AttnParams p) {
     if (m >= nrows) continue;
     const int64_t rowg = o0 + m / p.G;
     const int h = g * p.G + m % p.G;
-    const int64_t idx = partial_row(s, b, g, rt, m - m0, p.B, p.Hkv, p.row_tiles, p.tile_stride);
+    const int64_t idx = partial_slot(s, b, g, rt, m - m0, p.Hkv, p.row_tiles, p.tile_stride, p.splits);
     if (direct) {
       const float inv = l_run[r] > 0.f ? 1.f / l_run[r] : 0.f;
       const int64_t obase = (rowg * p.Hq + h) * D;
@@ -261,94 +263,13 @@ __global__ __launch_bounds__(128) void attn_simt_kernel(AttnParams p) {
       }
       continue;
     }
+    // partial O_s / l_s (fp32) with the split's running max and sum
+    const float inv = l_run[r] > 0.f ? 1.f / l_run[r] : 0.f;
     float4* dst = reinterpret_cast<float4*>(p.o_part + idx * D);
 #pragma unroll
-    for (int c = 0; c < CPL; ++c) dst[lane + 32 * c] = acc[r][c];
+    for (int c = 0; c < CPL; ++c)
+      dst[lane + 32 * c] = make_float4(acc[r][c].x * inv, acc[r][c].y * inv, acc[r][c].z * inv, acc[r][c].w * inv);
     if (lane == 0) p.ml_part[idx] = make_float2(m_run[r], l_run[r]);
-  }
-}
-
-// Combine the splits of every (row, head): one thread per 16-byte column
-// chunk of the output (D/4 threads per pair), so the partial rows of all
-// splits stream in parallel across the GPU.  In each warp, lane s reads split
-// s's (m, l), so the maxima and weights cost one round trip; the O loads of
-// up to 8 splits are then issued together.  More than 32 splits take
-// several passes with a running maximum.
-template <int D>
-__global__ __launch_bounds__(256, 2) void merge_kernel(MergeParams p) {
-  constexpr int TPP = D / 4;                       // threads per (row, head), a multiple of 32
-  constexpr int PPB = 256 / TPP;                   // pairs per block
-  constexpr int PF = 8;                            // O loads in flight per thread
-  const int lane = threadIdx.x & 31;
-  const int64_t pair = (int64_t)blockIdx.x * PPB + threadIdx.x / TPP;
-  const int c = threadIdx.x % TPP;
-  if (pair >= (int64_t)p.R * p.Hq) return;         // uniform over each warp (TPP % 32 == 0)
-  const int row = (int)(pair / p.Hq);
-  const int h = (int)(pair % p.Hq);
-  // sequence of this row: node_offsets is non-decreasing when valid
-  int lo = 0, hi = p.B - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (p.node_offsets[mid] <= row) lo = mid; else hi = mid - 1;
-  }
-  const int b = lo;
-  const bool valid = p.node_offsets[b] <= row && row < p.node_offsets[b + 1];
-  const int64_t P = clamp_prefix(p.prefix_len[b], p.max_prefix, p.capacity);
-  const int nch = valid ? num_chunks(P, p.chunk) : 0;
-  if (p.skip_single && nch == 1) return;           // the split pass wrote this row (uniform per pair)
-  // this (row, head) is query row m of its KV head's row tiles
-  const int m = (row - p.node_offsets[b]) * p.G + h % p.G;
-  const int rt = m / p.rows_per_tile, m_in = m - rt * p.rows_per_tile;
-  const int64_t r0 = partial_row(0, b, h / p.G, rt, m_in, p.B, p.Hkv, p.row_tiles, p.tile_stride);
-  const int64_t stride = partial_row(1, 0, 0, 0, 0, p.B, p.Hkv, p.row_tiles, p.tile_stride);   // per split
-  const float2* ml = p.ml_part + r0;
-  const float4* op = reinterpret_cast<const float4*>(p.o_part) + r0 * (D / 4) + c;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float L = 0.f, Mrun = -INFINITY;
-  for (int s0 = 0; s0 < nch; s0 += 32) {
-    const int ns = min(32, nch - s0);
-    const float2 mine = lane < ns ? ml[(int64_t)(s0 + lane) * stride] : make_float2(-INFINITY, 0.f);
-    float Mp = mine.x;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) Mp = fmaxf(Mp, __shfl_xor_sync(0xffffffffu, Mp, off));
-    const float Mnew = fmaxf(Mrun, Mp);
-    if (Mnew == -INFINITY) continue;               // every key so far masked
-    const float keep = Mrun == -INFINITY ? 0.f : exp2f(Mrun - Mnew);
-    acc.x *= keep; acc.y *= keep; acc.z *= keep; acc.w *= keep;
-    const float w = mine.x == -INFINITY ? 0.f : exp2f(mine.x - Mnew);
-    float lw = mine.y * w;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, off);
-    L = L * keep + lw;
-    Mrun = Mnew;
-    for (int t0 = 0; t0 < ns; t0 += PF) {
-      float4 v[PF];
-#pragma unroll
-      for (int t = 0; t < PF; ++t)
-        if (t0 + t < ns) v[t] = op[(int64_t)(s0 + t0 + t) * stride * (D / 4)];
-#pragma unroll
-      for (int t = 0; t < PF; ++t) {
-        const float wt = __shfl_sync(0xffffffffu, w, (t0 + t) & 31);
-        if (t0 + t < ns) {
-          acc.x = fmaf(wt, v[t].x, acc.x);
-          acc.y = fmaf(wt, v[t].y, acc.y);
-          acc.z = fmaf(wt, v[t].z, acc.z);
-          acc.w = fmaf(wt, v[t].w, acc.w);
-        }
-      }
-    }
-  }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  const float4 v = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-  const int64_t e = ((int64_t)row * p.Hq + h) * D + c * 4;
-  if (p.out_bf16) {
-    __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), bb = __floats2bfloat162_rn(v.z, v.w);
-    uint2 u;
-    u.x = *reinterpret_cast<uint32_t*>(&a);
-    u.y = *reinterpret_cast<uint32_t*>(&bb);
-    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) + e) = u;
-  } else {
-    *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + e) = v;
   }
 }
 
@@ -365,8 +286,7 @@ cudaError_t launch_simt_t(const AttnParams& p, cudaStream_t s) {
     configured = true;
   }
   dim3 grid(p.row_tiles * p.Hkv, p.splits, p.B);
-  attn_simt_kernel<T, D><<<grid, 128, smem, s>>>(p);
-  return cudaGetLastError();
+  return launch_dep(attn_simt_kernel<T, D>, grid, dim3(128), smem, s, p);
 }
 
 }  // namespace
@@ -382,14 +302,5 @@ cudaError_t launch_attn_simt(const AttnParams& p, int dtype, cudaStream_t s) {
   return launch_simt_t<__nv_bfloat16, 512>(p, s);
 }
 
-cudaError_t launch_merge(const MergeParams& p, cudaStream_t s) {
-  const int64_t pairs = (int64_t)p.R * p.Hq;
-  const int ppb = 256 / (p.d / 4);
-  const int blocks = (int)((pairs + ppb - 1) / ppb);
-  if (p.d == 128) merge_kernel<128><<<blocks, 256, 0, s>>>(p);
-  else if (p.d == 256) merge_kernel<256><<<blocks, 256, 0, s>>>(p);
-  else merge_kernel<512><<<blocks, 256, 0, s>>>(p);
-  return cudaGetLastError();
-}
 
 }  // namespace tv

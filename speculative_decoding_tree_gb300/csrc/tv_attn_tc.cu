@@ -65,7 +65,7 @@ struct Cfg {
   static constexpr int NS = D == 256 ? 5 : 6;     // ring slots
   static constexpr uint32_t Q_BYTES = BM * D * 2;
   static constexpr uint32_t RING_BYTES = NS * CHUNK_BYTES;
-  static constexpr int NBARS = 2 * NS + 13;
+  static constexpr int NBARS = 2 * NS + 12 + D / 32;   // ring, pipeline, epilogue boxes
   static constexpr uint32_t SMEM = kHeader + Q_BYTES + RING_BYTES;
   static_assert(NBARS * 8 + 8 <= 256, "barriers overflow the header");
   static_assert(SMEM <= 232448, "shared memory over the 227 KB per-block limit");
@@ -93,34 +93,6 @@ tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ 
   constexpr unsigned kAll = 0xffffffffu;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
 
-  // ---------------------------------------------------------------- work
-  const int rt = blockIdx.x;
-  const int g = blockIdx.y / p.splits;
-  const int s = blockIdx.y % p.splits;
-  const int b = blockIdx.z;
-  const int64_t Praw = p.prefix_len[b];            // read together with the offsets
-  int o0, n;
-  if (!seq_rows(p.node_offsets, b, p.R, p.max_nodes, p.status, &o0, &n)) return;
-  const int G = p.G;
-  const int nrows = n * G;
-  const int m0 = rt * p.rows_per_tile;
-  if (m0 >= nrows) return;
-  const int64_t P = clamp_prefix(Praw, p.max_prefix, p.capacity);
-  if (P != Praw && threadIdx.x == 0 && rt == 0 && s == 0 && g == 0) set_status(p.status, TV_DEV_BAD_PREFIX);
-  const int nch = num_chunks(P, p.chunk);
-  if (s >= nch) return;
-  // the layout below needs the dynamic shared window to start 1 KB aligned
-  if (smem_u32(smem_raw) & 1023u) {
-    if (threadIdx.x == 0) set_status(p.status, TV_DEV_TIMEOUT);
-    return;
-  }
-  const int64_t k_begin = (int64_t)s * p.chunk;
-  const int64_t k_end = min(P, k_begin + p.chunk);
-  const bool has_tree = (s == nch - 1);
-  const int npt = (int)((k_end - k_begin + BN - 1) / BN);      // prefix tiles
-  const int T = npt + (has_tree ? 1 : 0);
-  const int tail_valid = npt > 0 ? (int)(k_end - (k_begin + (int64_t)(npt - 1) * BN)) : BN;
-
   // ---------------------------------------------------------------- smem
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + C::NBARS * 8);
@@ -132,13 +104,22 @@ tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ 
   auto FULL = [&](int i) { return bar(i); };
   auto EMPTY = [&](int i) { return bar(NS + i); };
   const int bq = 2 * NS;
-  const uint32_t Q_FULL = bar(bq), TAIL = bar(bq + 7), FIN = bar(bq + 8), XL = bar(bq + 11), XST = bar(bq + 12);
+  const uint32_t Q_FULL = bar(bq), TAIL = bar(bq + 7), FIN = bar(bq + 8), XL = bar(bq + 11);
+  auto BOX = [&](int i) { return bar(bq + 12 + i); };     // epilogue box i staged (D / 32 boxes)
   auto S_FULL = [&](int i) { return bar(bq + 1 + i); };   // QK(t) done, buffer t & 1
   auto P_FULL = [&](int i) { return bar(bq + 3 + i); };   // softmax wrote P(t), buffer t & 1
   auto O_DONE = [&](int i) { return bar(bq + 5 + i); };   // PV(t) done, alternating by t & 1
   auto XCH = [&](int i) { return bar(bq + 9 + i); };      // row maxima exchanged for tile t, t & 1
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // the layout below needs the dynamic shared window to start 1 KB aligned
+  if (smem_u32(smem_raw) & 1023u) {
+    dep_wait();
+    if (tid == 0) set_status(p.status, TV_DEV_TIMEOUT);
+    return;
+  }
+  // on-chip setup before the dependency wait: it overlaps the previous
+  // kernel's tail when the launch is programmatic
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(FULL(i), 1);
@@ -154,7 +135,8 @@ tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ 
     mbar_init(TAIL, 1);
     mbar_init(FIN, 1);
     mbar_init(XL, kSoftmaxWarps);
-    mbar_init(XST, kSoftmaxWarps);
+    // box i: the 4 warps of one half, once per 32-column step it spans
+    for (int i = 0; i < D / 32; ++i) mbar_init(BOX(i), (p.part_bf16 ? 2 : 1) * (kSoftmaxWarps / 2));
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -171,19 +153,48 @@ tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ 
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_kc);
+    tma_prefetch_desc(&tm_vc);
+    tma_prefetch_desc(&tm_kt);
+    tma_prefetch_desc(&tm_vt);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  dep_wait();
+  dep_launch();
 
-  if (warp == 0) {
+  // ---------------------------------------------------------------- work
+  const int rt = blockIdx.x;
+  const int g = blockIdx.y / p.splits;
+  const int s = blockIdx.y % p.splits;
+  const int b = blockIdx.z;
+  const int64_t Praw = p.prefix_len[b];            // read together with the offsets
+  int o0 = 0, n = 1;
+  bool active = seq_rows(p.node_offsets, b, p.R, p.max_nodes, p.status, &o0, &n);
+  const int G = p.G;
+  const int nrows = n * G;
+  const int m0 = rt * p.rows_per_tile;
+  active = active && m0 < nrows;
+  const int64_t P = clamp_prefix(Praw, p.max_prefix, p.capacity);
+  if (active && P != Praw && tid == 0 && rt == 0 && s == 0 && g == 0) set_status(p.status, TV_DEV_BAD_PREFIX);
+  const int nch = num_chunks(P, p.chunk, p.tree_tile);
+  active = active && s < nch;                      // uniform over the CTA
+  const int64_t k_begin = (int64_t)s * p.chunk;
+  const int64_t k_end = min(P, k_begin + p.chunk);
+  const bool has_tree = (s == nch - 1);
+  const int npt = (int)((k_end - k_begin + BN - 1) / BN);      // prefix tiles
+  const int T = npt + (has_tree ? 1 : 0);
+  const int tail_valid = npt > 0 ? (int)(k_end - (k_begin + (int64_t)(npt - 1) * BN)) : BN;
+
+  if (!active) {
+    // nothing to do for this CTA: straight to teardown
+  } else if (warp == 0) {
     // ============================================================ producer
     if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_kc);
-      tma_prefetch_desc(&tm_vc);
-      tma_prefetch_desc(&tm_kt);
-      tma_prefetch_desc(&tm_vt);
       mbar_expect_tx(Q_FULL, (uint32_t)p.rows_per_tile * 128u * (D / 64));
       for (int kb = 0; kb < D / 64; ++kb)
         tma_load_3d(smem_u32(sQ + kb * (BM * 128)), &tm_q, Q_FULL, kb * 64, g * G, o0 + m0 / G);
@@ -330,6 +341,30 @@ tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ 
       mma_commit(FIN);
       mbar_wait(FIN, 0, abort_flag, kWaitNs);
     }
+  } else if (warp == 2) {
+    // ============================================================ partials store
+    // one 128-byte-wide box of the partial tile at a time (32 fp32 or 64 bf16
+    // columns), as soon as the softmax warps of its half have staged it;
+    // every box barrier is arrived in all paths, so the waits here end
+    if (lane == 0) {
+      const bool store = !(p.out != nullptr && nch == 1);
+      const int row0 = (int)(((int64_t)b * p.Hkv + g) * p.row_tiles + rt) * BM;   // first row of the tile
+      const int cols = p.part_bf16 ? 64 : 32;     // columns per box
+      const int per_half = (D / 2) / cols;
+      bool issued = false;
+      for (int j = 0; j < per_half; ++j) {
+        for (int hf = 0; hf < 2; ++hf) {
+          const int bx = hf * per_half + j;
+          const bool in = mbar_wait(BOX(bx), 0, abort_flag, kWaitNs);
+          if (in && store && !*abort_flag) {
+            tma_store_3d(&tm_op, smem_u32(ring + bx * (BM * 128)), hf * (D / 2) + j * cols, s, row0);
+            bulk_commit_group();
+            issued = true;
+          }
+        }
+      }
+      if (issued) bulk_wait_read_all();
+    }
   } else if (warp >= 4) {
     // ============================================================ softmax
     // Two warpgroups: `half` 0 takes keys 0-63 of every tile (and O columns
@@ -432,31 +467,36 @@ tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ 
     // epilogue: the last P V has landed (its commit covers every earlier
     // MMA); add the two halves' sums.  A sequence with one chunk writes its
     // normalised rows directly (the merge's arithmetic for one split).
-    // Otherwise the fp32 tile goes through shared memory (the ring, idle
-    // now; 128-byte swizzled 32-column boxes) and out with TMA stores into
-    // this CTA's own tile of the partials.
+    // Otherwise the partial O_s / l_s (fp32, or bf16 with a bf16 output) is
+    // staged in the ring (idle now; 128-byte swizzled boxes), each box's
+    // barrier arrived as soon as it is written (in every path, so warp 2's
+    // waits always end), and warp 2 stores the boxes into this CTA's tile.
     const int u = T - 1;
     const bool direct = p.out != nullptr && nch == 1;
-    const int64_t tile = partial_row(s, b, g, rt, 0, p.B, p.Hkv, p.row_tiles, BM) / BM;
-    bool staged = false;
-    if (ok && __all_sync(kAll, mbar_wait(O_DONE(u & 1), (u >> 1) & 1, abort_flag, kWaitNs))) {
+    const bool epi = ok && __all_sync(kAll, mbar_wait(O_DONE(u & 1), (u >> 1) & 1, abort_flag, kWaitNs));
+    bool got = false;
+    float lsum = 0.f;
+    if (epi) {
       tc_fence_after();
       float* xb = xch + (T & 1) * 256;
       xb[half * 128 + r] = l;
       __syncwarp();
       if (lane == 0) mbar_arrive(XL);
-      const bool got = __all_sync(kAll, mbar_wait(XL, 0, abort_flag, kWaitNs));
-      const float lsum = l + xb[(half ^ 1) * 128 + r];
-      const int64_t rowg = o0 + node;
-      const int h = g * G + (m0 + r) % G;
-      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+      got = __all_sync(kAll, mbar_wait(XL, 0, abort_flag, kWaitNs));
+      lsum = l + xb[(half ^ 1) * 128 + r];
+    }
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    const int64_t rowg = o0 + node;
+    const int h = g * G + (m0 + r) % G;
 #pragma unroll 1
-      for (int q = 0; q < D / 64; ++q) {
-        uint32_t rr[32];
-        tmem_ld_x32(tmem + lane_base + 256 + half * (D / 2) + q * 32, rr);
-        if (!got) continue;
-        if (direct) {
-          if (!row_ok) continue;
+    for (int qq = 0; qq < D / 128; ++qq) {         // 64 columns per TMEM load, two 32-column steps
+      uint32_t rv[64];
+      if (epi) tmem_ld_x64(tmem + lane_base + 256 + half * (D / 2) + qq * 64, rv);
+#pragma unroll
+      for (int sub = 0; sub < 2; ++sub) {
+        const int q = 2 * qq + sub;
+        const uint32_t* rr = rv + 32 * sub;
+        if (epi && got && direct && row_ok) {
           const int64_t e = (rowg * p.Hq + h) * D + half * (D / 2) + q * 32;
           if (p.out_bf16) {
             uint4* ob = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + e);
@@ -476,34 +516,38 @@ tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ 
               of[e4] = make_float4(__uint_as_float(rr[4 * e4]) * inv, __uint_as_float(rr[4 * e4 + 1]) * inv,
                                    __uint_as_float(rr[4 * e4 + 2]) * inv, __uint_as_float(rr[4 * e4 + 3]) * inv);
           }
-        } else {
-          // box (half * D/64 + q): 128 rows x 128 bytes, 16-byte chunk c of
-          // row r at chunk c ^ (r & 7)
-          uint8_t* box = ring + (uint32_t)(half * (D / 64) + q) * (BM * 128) + r * 128;
+        } else if (epi && got && !direct) {
+          // row r of the partial O_s / l_s: 128-byte box rows, 16-byte chunk
+          // c at chunk c ^ (r & 7)
+          if (p.part_bf16) {                       // 64 columns per box: this step fills half a row
+            uint8_t* box = ring + (uint32_t)(half * (D / 128) + qq) * (BM * 128) + r * 128;
 #pragma unroll
-          for (int c4 = 0; c4 < 8; ++c4)
-            *reinterpret_cast<uint4*>(box + ((c4 ^ (r & 7)) * 16)) =
-                make_uint4(rr[4 * c4], rr[4 * c4 + 1], rr[4 * c4 + 2], rr[4 * c4 + 3]);
+            for (int c4 = 0; c4 < 4; ++c4) {
+              uint4 w4;
+              w4.x = pack_bf16(__uint_as_float(rr[8 * c4 + 0]) * inv, __uint_as_float(rr[8 * c4 + 1]) * inv);
+              w4.y = pack_bf16(__uint_as_float(rr[8 * c4 + 2]) * inv, __uint_as_float(rr[8 * c4 + 3]) * inv);
+              w4.z = pack_bf16(__uint_as_float(rr[8 * c4 + 4]) * inv, __uint_as_float(rr[8 * c4 + 5]) * inv);
+              w4.w = pack_bf16(__uint_as_float(rr[8 * c4 + 6]) * inv, __uint_as_float(rr[8 * c4 + 7]) * inv);
+              *reinterpret_cast<uint4*>(box + (((sub * 4 + c4) ^ (r & 7)) * 16)) = w4;
+            }
+          } else {                                 // 32 fp32 columns per box
+            uint8_t* box = ring + (uint32_t)(half * (D / 64) + q) * (BM * 128) + r * 128;
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4)
+              *reinterpret_cast<uint4*>(box + ((c4 ^ (r & 7)) * 16)) =
+                  make_uint4(__float_as_uint(__uint_as_float(rr[4 * c4]) * inv),
+                             __float_as_uint(__uint_as_float(rr[4 * c4 + 1]) * inv),
+                             __float_as_uint(__uint_as_float(rr[4 * c4 + 2]) * inv),
+                             __float_as_uint(__uint_as_float(rr[4 * c4 + 3]) * inv));
+          }
         }
-      }
-      if (!direct && got) {
-        p.ml_part[tile * BM + r] = make_float2(row_ok ? m_ref : -INFINITY, row_ok ? lsum : 0.f);
-        staged = true;
-      }
-    }
-    // every softmax thread arrives (staged or not); one issues the stores
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(XST);
-    if (tid == 128) {
-      const bool all_in = mbar_wait(XST, 0, abort_flag, kWaitNs);
-      if (all_in && !direct && !*abort_flag) {
-        for (int bx = 0; bx < D / 32; ++bx) tma_store_2d(&tm_op, smem_u32(ring + bx * (BM * 128)), bx * 32, (int)(tile * BM));
-        bulk_commit_group();
-        bulk_wait_all();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BOX(p.part_bf16 ? half * (D / 128) + qq : half * (D / 64) + q));
       }
     }
-    (void)staged;
+    if (epi && got && !direct)
+      p.ml_part[partial_slot(s, b, g, rt, r, p.Hkv, p.row_tiles, BM, p.splits)] = make_float2(row_ok ? m_ref : -INFINITY, row_ok ? lsum : 0.f);
   }
 
   // ---------------------------------------------------------------- teardown
@@ -576,12 +620,16 @@ cudaError_t launch_tc_t(const AttnParams& p, cudaStream_t st) {
   }
   CUtensorMap mop;
   {
-    // partials: [tiles * 128 rows, D] fp32, stored as 32-column boxes
-    const cuuint64_t tiles = (cuuint64_t)p.splits * p.B * p.Hkv * p.row_tiles;
-    cuuint64_t dims[2] = {(cuuint64_t)D, tiles * BM};
-    cuuint64_t strides[1] = {(cuuint64_t)D * 4};
-    cuuint32_t box[2] = {32, BM};
-    if (!encode(&mop, p.o_part, 2, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32)) return cudaErrorInvalidValue;
+    // partials [rows][splits][D] (partial_slot), fp32 (boxes of 32 columns)
+    // or bf16 (64); a CTA stores one split of a 128-row tile
+    const cuuint64_t es = p.part_bf16 ? 2 : 4;
+    const cuuint64_t rows = (cuuint64_t)p.B * p.Hkv * p.row_tiles * BM;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.splits, rows};
+    cuuint64_t strides[2] = {(cuuint64_t)D * es, (cuuint64_t)D * es * p.splits};
+    cuuint32_t box[3] = {p.part_bf16 ? 64u : 32u, 1u, BM};
+    if (!encode(&mop, p.o_part, 3, dims, strides, box,
+                p.part_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
+      return cudaErrorInvalidValue;
   }
   static bool configured = false;
   if (!configured) {
@@ -591,8 +639,7 @@ cudaError_t launch_tc_t(const AttnParams& p, cudaStream_t st) {
     configured = true;
   }
   dim3 grid(p.row_tiles, p.Hkv * p.splits, p.B);
-  tv_attn_tc_kernel<D><<<grid, kThreads, Cfg<D>::SMEM, st>>>(p, mq, mkc, mvc, mkt, mvt, mop);
-  return cudaGetLastError();
+  return launch_dep(tv_attn_tc_kernel<D>, grid, dim3(kThreads), Cfg<D>::SMEM, st, p, mq, mkc, mvc, mkt, mvt, mop);
 }
 
 }  // namespace

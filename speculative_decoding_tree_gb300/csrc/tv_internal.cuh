@@ -26,9 +26,10 @@ struct AttnParams {
   const void* k_tree;        // [Hkv, R, d]
   const void* v_tree;
   const uint64_t* anc;       // [R]
-  float* o_part;             // [tiles, tile_stride, d]  unnormalised partial output, tile-major:
-                             // tile = ((split * B + b) * Hkv + g) * row_tiles + row_tile
-  float2* ml_part;           // [tiles, tile_stride]     (running max in log2 units, running sum)
+  float* o_part;             // [slots, d] partial output O_s / l_s at partial_slot(); fp32, or
+                             // bf16 when part_bf16 (then the rows are d bf16 wide)
+  float2* ml_part;           // [slots] (running max in log2 units, running sum)
+  int part_bf16;             // partials stored as bf16 (tensor-core kernels with bf16 output)
   void* out;                 // [R, Hq, d] or nullptr: a sequence with one key chunk writes its
                              // normalised rows here instead of partials (the merge skips it)
   int out_bf16;
@@ -38,38 +39,58 @@ struct AttnParams {
   int64_t capacity, num_pages, max_pages, max_prefix;
   float scale_log2;          // softmax scale * log2(e): scores are kept in base-2 units
   int chunk;                 // keys per split (multiple of the kernel's key tile)
+  int tree_tile;             // 0, or the key tile when the tree may take a split of its own (num_chunks)
   int splits;                // splits in the grid (covers max_prefix)
   int rows_per_tile;         // query rows per row tile (node x group head)
   int row_tiles;
   int tile_stride;           // partial rows reserved per tile (>= rows_per_tile)
 };
 
-// Partial-row index of query row m_in of row tile rt of (split, b, g).
-__host__ __device__ inline int64_t partial_row(int split, int b, int g, int rt, int m_in, int B, int Hkv,
-                                               int row_tiles, int tile_stride) {
-  return ((((int64_t)split * B + b) * Hkv + g) * row_tiles + rt) * tile_stride + m_in;
+// Slot of the partial of query row m_in of row tile rt of (sequence b, KV
+// head g) from split s.  The splits of one row are adjacent, and the rows of
+// a row tile follow each other, so the partials a merge CTA combines (a slab
+// of rows, every split) are one contiguous block.
+__host__ __device__ inline int64_t partial_slot(int s, int b, int g, int rt, int m_in, int Hkv, int row_tiles,
+                                                int tile_stride, int splits) {
+  return ((((int64_t)b * Hkv + g) * row_tiles + rt) * tile_stride + m_in) * splits + s;
 }
 
 struct MergeParams {
   const int32_t* prefix_len;
   const int32_t* node_offsets;
-  const float* o_part;
+  const float* o_part;       // fp32 or (part_bf16) bf16 rows of d values
   const float2* ml_part;
+  int part_bf16;
   void* out;
   int32_t* status;
   int B, Hq, d, R, max_nodes, out_bf16;
   int skip_single;           // rows of one-chunk sequences were written by the split pass
   int Hkv, G, rows_per_tile, row_tiles, tile_stride;
   int64_t max_prefix, capacity;
-  int chunk, splits;
+  int chunk, tree_tile, splits;
+  int slab_rows;             // rows per merge CTA (2..16, even, <= tile_stride)
+  int batch_splits;          // splits gathered into shared memory at once
 };
 
-// Number of key chunks sequence b is split into, from its (clamped) prefix
-// length.  The last chunk also takes the tree keys.  Host and device use the
-// same formula so the merge reads exactly the partials the split pass wrote.
-__host__ __device__ inline int num_chunks(int64_t P, int chunk) {
+// Merge CTA shape for `tiles` (sequence, KV head, row tile) triples.
+void merge_shape(int tiles, int tile_stride, int d, int esize, int splits, int sms, int* slab_rows,
+                 int* batch_splits);
+
+// Number of key chunks (splits) of a sequence with a (clamped) prefix of P
+// keys: the prefix in chunks of `chunk` keys, the tree keys with the last of
+// them.  With tree_tile > 0 (one-wave plans) and a prefix of two or more
+// chunks, the tree gets a split of its own when the last prefix chunk already
+// has chunk / tree_tile key tiles, so that no split has more tiles than a full
+// chunk.  Host and device use the same formula, so the merge reads exactly the
+// partials the split pass wrote; it never decreases as P grows.
+__host__ __device__ inline int num_chunks(int64_t P, int chunk, int tree_tile) {
   int64_t n = (P + chunk - 1) / chunk;
-  return n < 1 ? 1 : (int)n;
+  if (n < 1) return 1;
+  if (tree_tile > 0 && n >= 2) {
+    const int64_t last = P - (n - 1) * chunk;
+    if ((last + tree_tile - 1) / tree_tile >= chunk / tree_tile) ++n;
+  }
+  return (int)n;
 }
 
 __host__ __device__ inline int64_t clamp_prefix(int64_t P, int64_t max_prefix, int64_t capacity) {
@@ -95,6 +116,33 @@ __device__ inline bool seq_rows(const int32_t* offs, int b, int R, int max_nodes
   *o0 = a;
   *n = cnt;
   return true;
+}
+
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with programmatic stream serialization, so its CTAs may start while the
+// previous kernel of the stream is still running.  Each kernel therefore
+// touches no global memory before dep_wait(), which returns once the previous
+// grid has completed and its writes are visible; every CTA calls it, so a
+// grid never completes before its predecessor and the ordering of the whole
+// stream stays transitive.  dep_launch() lets the next kernel's CTAs be
+// scheduled early (they wait in dep_wait for this grid to finish).
+__device__ __forceinline__ void dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dep(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
 // Launchers (return cudaError_t of the launch).

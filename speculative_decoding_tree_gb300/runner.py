@@ -83,5 +83,8 @@ class DeviceStep:
         self.attn(stream)
         self.accept_commit(stream)
 
-    # launches of our kernels in one step (mask 1, split 1, merge 1, argmax 1, walk+commit 1)
-    KERNELS_PER_STEP = 5
+    def kernels_per_step(self):
+        """Our kernel launches in one step: mask, split, merge (skipped when
+        the plan has one key chunk), argmax, walk + commit."""
+        from . import tv_attn_plan
+        return 4 + (1 if tv_attn_plan(self.desc)["num_splits"] > 1 else 0)

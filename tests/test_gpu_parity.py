@@ -61,3 +61,25 @@ def test_bf16_out_f32():
     st = run(w, out_f32=True)
     assert st.out.dtype == torch.float32
     check_step(w, st, oracle.verify_step(w))
+
+
+@pytest.mark.parametrize("P", [1, 512, 513, 1024, 3584, 3585, 3968, 3969, 4096])
+def test_tree_split_rule(P):
+    # one plan (one wave) for prefixes up to 4096; the device
+    # prefix decides per sequence whether the tree joins the last chunk or
+    # gets a split of its own, and how many splits the merge combines
+    spec = wl.CONFIGS[3].replace(prefix=(P, P), vocab=300, tree="random:13,13,5", seed=500 + P,
+                                 cache_margin=4200 - P)
+    w = workload(spec)
+    check_step(w, run(w, max_prefix=4096), oracle.verify_step(w))
+
+
+def test_merge_in_batches():
+    # one KV head, head_dim 512: more splits than one merge batch holds in
+    # shared memory, so the merge keeps a running maximum across batches
+    spec = wl.CONFIGS[2].replace(hq=8, hkv=1, prefix=(20000, 20000), vocab=300, seed=4242)
+    w = workload(spec)
+    st = run(w)
+    from speculative_decoding_tree_gb300 import tv_attn_plan
+    assert tv_attn_plan(st.desc)["num_splits"] > 24
+    check_step(w, st, oracle.verify_step(w))
