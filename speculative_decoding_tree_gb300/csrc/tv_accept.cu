@@ -200,23 +200,43 @@ __global__ __launch_bounds__(256) void argmax_partial_kernel(const void* __restr
 
 // ----------------------------------------------------------------- A4 + A5
 
-// One block per sequence.  Warp 0 finishes the argmax of every node, builds
-// ancestors and depths, and walks (lane i owns nodes i and i + 32; ballots
-// and shuffles, no shared atomics); then the whole block copies the accepted
-// rows' K/V into the cache and advances prefix_len.
+// One block per sequence.  The block finishes the argmax of every node from
+// its chunk partials (four threads per node); warp 0 builds ancestors and
+// depths and walks (lane i owns nodes i and i + 32; ballots and shuffles, no
+// shared atomics); then each warp copies whole accepted K/V rows into the
+// cache, and thread 0 advances prefix_len.
+constexpr int kCommitPages = kMaxNodes / kPageSize + 1;   // pages the k + 1 <= 64 rows can touch
+
 __global__ __launch_bounds__(256) void walk_commit_kernel(AcceptParams p) {
   __shared__ int s_par[kMaxNodes], s_draft[kMaxNodes], s_am[kMaxNodes], s_path[kMaxNodes];
   __shared__ uint64_t s_anc[kMaxNodes];
-  __shared__ float s_pv[kMaxNodes * kMaxVChunks];
-  __shared__ int s_pi[kMaxNodes * kMaxVChunks];
-  __shared__ int s_P, s_k, s_ok;
+  __shared__ int s_pid[kCommitPages];
+  __shared__ int s_k, s_ok;
 
-  dep_wait();
-  dep_launch();
   const int b = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  int o0, n;
-  if (!seq_rows(p.node_offsets, b, p.R, p.max_nodes, p.status, &o0, &n)) {
+  // The sequence's lengths, parents, drafts and pages come from before the
+  // argmax pass (which writes none of them and waited for its own
+  // predecessor before letting this kernel start), so they are read before
+  // the dependency wait; only the argmax partials wait for it.
+  int o0 = 0, n = 0;
+  const bool valid = seq_rows(p.node_offsets, b, p.R, p.max_nodes, nullptr, &o0, &n);
+  const int P = valid ? p.prefix_len[b] : 0;
+  if (valid) {
+    if (tid < n) {
+      s_par[tid] = p.parents[o0 + tid];
+      s_draft[tid] = p.draft[o0 + tid];
+    }
+    // page ids of the positions P .. P + n - 1 a commit may write
+    if (p.paged && tid >= 64 && tid < 64 + kCommitPages && P >= 0) {
+      const int64_t pg = (int64_t)P / kPageSize + (tid - 64);
+      s_pid[tid - 64] = pg < p.max_pages ? p.page_table[(int64_t)b * p.max_pages + pg] : -1;
+    }
+  }
+  dep_wait();
+  dep_launch();
+  if (!valid) {
+    if (tid == 0) set_status(p.status, TV_DEV_BAD_OFFSETS);
     if (tid < p.max_nodes) {
       p.path[(int64_t)b * p.max_nodes + tid] = -1;
       p.tokens[(int64_t)b * p.max_nodes + tid] = -1;
@@ -224,35 +244,32 @@ __global__ __launch_bounds__(256) void walk_commit_kernel(AcceptParams p) {
     if (tid == 0) p.accept_len[b] = -1;
     return;
   }
-  // every global read the walk needs, issued together
-  const int vc = p.vchunks;
-  if (tid == 0) s_P = p.prefix_len[b];
-  if (tid < n) {
-    s_par[tid] = p.parents[o0 + tid];
-    s_draft[tid] = p.draft[o0 + tid];
-  }
-  for (int e = tid; e < n * vc; e += blockDim.x) {
-    s_pv[e] = p.am_val[(int64_t)o0 * vc + e];
-    s_pi[e] = p.am_idx[(int64_t)o0 * vc + e];
+  // argmax of node tid / 4 from chunks c = tid % 4, + 4, ...; max value,
+  // smallest index (better() is order-free), NaN never enters
+  {
+    const int vc = p.vchunks;
+    const int i = tid >> 2;
+    Best bst{-FLT_MAX, -1};
+    if (i < n)
+      for (int c = tid & 3; c < vc; c += 4)
+        bst = better(bst, Best{p.am_val[(int64_t)(o0 + i) * vc + c], p.am_idx[(int64_t)(o0 + i) * vc + c]});
+#pragma unroll
+    for (int off = 1; off < 4; off <<= 1) {
+      Best o;
+      o.v = __shfl_xor_sync(0xffffffffu, bst.v, off);
+      o.i = __shfl_xor_sync(0xffffffffu, bst.i, off);
+      bst = better(bst, o);
+    }
+    if (i < n && (tid & 3) == 0) {
+      const int am = bst.i < 0 ? 0 : bst.i;
+      s_am[i] = am;
+      p.argmax[o0 + i] = am;
+    }
   }
   __syncthreads();
 
   if (warp == 0) {
     const unsigned all = 0xffffffffu;
-    // argmax of each node from its chunk partials (ascending chunk order
-    // keeps the smallest index on ties)
-#pragma unroll
-    for (int hlf = 0; hlf < 2; ++hlf) {
-      const int i = lane + 32 * hlf;
-      if (i < n) {
-        Best bst{-FLT_MAX, -1};
-        for (int c = 0; c < vc; ++c) bst = better(bst, Best{s_pv[i * vc + c], s_pi[i * vc + c]});
-        const int am = bst.i < 0 ? 0 : bst.i;
-        s_am[i] = am;
-        p.argmax[o0 + i] = am;
-      }
-    }
-    __syncwarp();
     // ancestors and depth by walking parents; validate; match against the
     // parent's argmax
     uint64_t anc[2] = {0ull, 0ull};
@@ -320,7 +337,6 @@ __global__ __launch_bounds__(256) void walk_commit_kernel(AcceptParams p) {
       }
     }
     // can the k+1 rows be committed?
-    const int P = s_P;
     bool ok = true;
     if (P < 0) {
       ok = false;
@@ -334,8 +350,7 @@ __global__ __launch_bounds__(256) void walk_commit_kernel(AcceptParams p) {
       for (int hlf = 0; hlf < 2; ++hlf) {
         const int t = lane + 32 * hlf;
         if (t <= k) {
-          const int64_t pos = (int64_t)P + t;
-          const int pid = p.page_table[(int64_t)b * p.max_pages + pos / kPageSize];
+          const int pid = s_pid[(P + t) / kPageSize - P / kPageSize];
           page_bad |= (pid < 0 || pid >= p.num_pages);
         }
       }
@@ -352,45 +367,55 @@ __global__ __launch_bounds__(256) void walk_commit_kernel(AcceptParams p) {
   }
   __syncthreads();
   if (!s_ok) return;
-  const int P = s_P, k = s_k;
-  // copy k+1 rows x Hkv heads of K and of V in 16-byte units: each thread
-  // loads all its units first, then stores them (the loads do not wait on
-  // the stores, which the compiler cannot prove independent)
-  const int units_row = p.d * p.esize / 16;
-  const int per_kind = (k + 1) * p.Hkv;
-  const int total = 2 * per_kind * units_row;
-  constexpr int U = 8;
-  for (int base = 0; base < total; base += U * (int)blockDim.x) {
-    uint4 v[U];
-    uint4* dst[U];
+  const int k = s_k;
+  // copy k+1 rows x Hkv heads of K and of V: warp w takes rows w, w + 8, ...
+  // of the list (K or V, t, head), eight at a time, lane u moving 16-byte
+  // units u, u + 32, ... of each; a batch's loads are all issued before its
+  // stores (the compiler cannot prove them independent)
+  const int64_t row_bytes = (int64_t)p.d * p.esize;
+  const int units_row = (int)(row_bytes / 16);
+  const int kh = (k + 1) * p.Hkv, nrow = 2 * kh;
+  constexpr int RB = 8;
+  for (int r0 = warp; r0 < nrow; r0 += 8 * RB) {
+    // (kind, t, g) of row r0, then advanced 8 rows at a time
+    int kind = r0 / kh, rem = r0 - kind * kh, t = rem / p.Hkv, g = rem - t * p.Hkv;
+    const uint4* src[RB];
+    uint4* dst[RB];
 #pragma unroll
-    for (int q = 0; q < U; ++q) {
-      const int u = base + q * (int)blockDim.x + tid;
-      dst[q] = nullptr;
-      if (u < total) {
-        const int rr = u / units_row, cu = u - rr * units_row;
-        const int which = rr / per_kind;            // 0 = K, 1 = V
-        const int rem = rr - which * per_kind;
-        const int t = rem / p.Hkv, g = rem - t * p.Hkv;
-        const int node = s_path[t];
-        const uint4* src = reinterpret_cast<const uint4*>(
-            reinterpret_cast<const char*>(which ? p.v_tree : p.k_tree) + (((int64_t)g * p.R + o0 + node) * p.d) * p.esize);
+    for (int j = 0; j < RB; ++j) {
+      src[j] = nullptr;
+      dst[j] = nullptr;
+      if (kind < 2) {
         const int64_t pos = (int64_t)P + t;
         int64_t drow;
         if (p.paged) {
-          const int pid = p.page_table[(int64_t)b * p.max_pages + pos / kPageSize];
+          const int pid = s_pid[(P + t) / kPageSize - P / kPageSize];
           drow = ((int64_t)pid * p.Hkv + g) * kPageSize + pos % kPageSize;
         } else {
           drow = ((int64_t)b * p.Hkv + g) * p.capacity + pos;
         }
-        v[q] = src[cu];
-        dst[q] = reinterpret_cast<uint4*>(reinterpret_cast<char*>(which ? p.v_cache : p.k_cache) +
-                                          drow * p.d * p.esize) + cu;
+        src[j] = reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(kind ? p.v_tree : p.k_tree) +
+                                                ((int64_t)g * p.R + o0 + s_path[t]) * row_bytes);
+        dst[j] = reinterpret_cast<uint4*>(reinterpret_cast<char*>(kind ? p.v_cache : p.k_cache) + drow * row_bytes);
+        g += 8;                                     // next row of this warp
+        while (g >= p.Hkv) {
+          g -= p.Hkv;
+          if (++t > k) {
+            t = 0;
+            ++kind;
+          }
+        }
       }
     }
+    for (int u = lane; u < units_row; u += 32) {
+      uint4 v[RB];
 #pragma unroll
-    for (int q = 0; q < U; ++q)
-      if (dst[q]) *dst[q] = v[q];
+      for (int j = 0; j < RB; ++j)
+        if (src[j]) v[j] = src[j][u];
+#pragma unroll
+      for (int j = 0; j < RB; ++j)
+        if (dst[j]) dst[j][u] = v[j];
+    }
   }
   __syncthreads();
   if (tid == 0) p.prefix_len[b] = P + k + 1;

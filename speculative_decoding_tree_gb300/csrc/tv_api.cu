@@ -219,6 +219,7 @@ int launch_merge_from(const tv_desc* d, const Plan& pl, const int32_t* plen, con
                       const void* ws, int32_t* st, cudaStream_t s, int skip_single) {
   MergeParams m;
   m.skip_single = skip_single;
+  m.early_reads = skip_single;    // tree_verify_attn: the split pass of this call precedes the merge
   m.prefix_len = plen; m.node_offsets = no;
   m.o_part = reinterpret_cast<const float*>(ws);
   m.ml_part = reinterpret_cast<const float2*>(reinterpret_cast<const char*>(ws) + pl.o_part_bytes);

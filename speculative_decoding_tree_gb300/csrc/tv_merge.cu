@@ -54,12 +54,30 @@ __global__ __launch_bounds__(kMergeThreads) void merge_slab_kernel(MergeParams p
     fence_barrier_init();
   }
   __syncthreads();
-  dep_wait();
-  dep_launch();
 
   const int b = blockIdx.z;
   const int g = blockIdx.y / p.row_tiles, rt = blockIdx.y % p.row_tiles;
   const int r0 = blockIdx.x * RS;                   // first row of the slab inside the tile
+  // Launched right after the split pass of the same call (early_reads), the
+  // sequence's lengths are read before the dependency wait: the split pass
+  // does not write them and waited for its own predecessor before letting
+  // this kernel start.  Only the partials wait for it.
+  if (!p.early_reads) dep_wait();
+  const int64_t Praw = p.prefix_len[b];
+  int o0 = 0, n = 1;
+  const bool valid = seq_rows(p.node_offsets, b, p.R, p.max_nodes, nullptr, &o0, &n);
+  const int nrows = n * p.G;
+  const int m_first = rt * p.rows_per_tile + r0;
+  const int64_t P = clamp_prefix(Praw, p.max_prefix, p.capacity);
+  const int nch = num_chunks(P, p.chunk, p.tree_tile);
+  // rows this CTA writes (none: empty slab, or the split pass wrote them)
+  const bool live = valid && r0 < p.rows_per_tile && m_first < nrows && !(p.skip_single && nch == 1);
+  const int rows = live ? min(RS, min(p.rows_per_tile - r0, nrows - m_first)) : 0;
+  dep_wait();
+  dep_launch();
+  if (!valid && tid == 0) set_status(p.status, TV_DEV_BAD_OFFSETS);
+  if (!live) return;
+
   const int crow = min(RS, p.tile_stride - r0);     // rows gathered (inside the tile)
   const int64_t slot0 = partial_slot(0, b, g, rt, r0, p.Hkv, p.row_tiles, p.tile_stride, S);
   const PT* src = reinterpret_cast<const PT*>(p.o_part);
@@ -78,21 +96,7 @@ __global__ __launch_bounds__(kMergeThreads) void merge_slab_kernel(MergeParams p
                     (uint32_t)(nb * D * sizeof(PT)), bar_a);
     }
   };
-  // the first batch goes out before the sequence's lengths are known (the
-  // workspace holds every split of every slab; splits past the sequence's
-  // own count are read and ignored)
   gather(0, min(SB, S));
-
-  const int64_t Praw = p.prefix_len[b];
-  int o0 = 0, n = 1;
-  bool live = seq_rows(p.node_offsets, b, p.R, p.max_nodes, p.status, &o0, &n);
-  const int nrows = n * p.G;
-  const int m_first = rt * p.rows_per_tile + r0;
-  live = live && r0 < p.rows_per_tile && m_first < nrows;
-  const int64_t P = clamp_prefix(Praw, p.max_prefix, p.capacity);
-  const int nch = num_chunks(P, p.chunk, p.tree_tile);
-  live = live && !(p.skip_single && nch == 1);      // else the split pass wrote these rows
-  const int rows = live ? min(RS, min(p.rows_per_tile - r0, nrows - m_first)) : 0;
 
   constexpr int C4 = D / 4;                         // float4 columns per row
   const int items = rows * C4;
@@ -106,7 +110,7 @@ __global__ __launch_bounds__(kMergeThreads) void merge_slab_kernel(MergeParams p
   }
   bool ok = true;
   int phase = 0;
-  for (int s0 = 0; live && s0 < nch && ok; s0 += SB, ++phase) {
+  for (int s0 = 0; s0 < nch && ok; s0 += SB, ++phase) {
     const int nb = min(SB, nch - s0);
     if (s0 > 0) gather(s0, min(SB, S - s0));
     for (int e = tid; e < rows * nb; e += kMergeThreads) {   // (m, l) of the batch, plain loads
@@ -162,11 +166,10 @@ __global__ __launch_bounds__(kMergeThreads) void merge_slab_kernel(MergeParams p
     }
     __syncthreads();                                // the next batch overwrites the buffers
   }
-  if (!live || !ok) {
-    // nothing to write, or a copy that never landed: flag the latter, and
-    // give the copies in flight a bounded time to finish before the CTA (and
-    // its shared memory) ends
-    if (!ok && tid == 0) set_status(p.status, TV_DEV_TIMEOUT);
+  if (!ok) {
+    // a copy that never landed: flag it, and give the copies in flight a
+    // bounded time to finish before the CTA (and its shared memory) ends
+    if (tid == 0) set_status(p.status, TV_DEV_TIMEOUT);
     int spare = 0;
     mbar_wait(bar_a, phase & 1, &spare, kMergeWaitNs);
     return;
