@@ -88,3 +88,39 @@ class DeviceStep:
         the plan has one key chunk), argmax, walk + commit."""
         from . import tv_attn_plan
         return 4 + (1 if tv_attn_plan(self.desc)["num_splits"] > 1 else 0)
+
+
+def main(argv=None):
+    """Run one seeded input set of a workload through the verify step a few
+    times (e.g. under a profiler): python -m speculative_decoding_tree_gb300.runner
+    --config 4 --steps 3.  Prints the device status word and exits non-zero
+    when it is not 0."""
+    import argparse
+
+    from . import _build, workloads as wl
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--config", type=int, default=4, help="workload 1..5")
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--attn-only", action="store_true", help="mask and attention only")
+    a = ap.parse_args(argv)
+    _build.build()
+    w = wl.make_workload(wl.CONFIGS[a.config], canary=0.0,
+                         argmax_fn=lambda x: torch.argmax(x.float(), dim=1))   # plants the draft tokens
+    st = DeviceStep(w)
+    p0 = st.prefix_len.clone()
+    for _ in range(a.steps):
+        st.prefix_len.copy_(p0)
+        if a.attn_only:
+            st.mask()
+            st.attn()
+        else:
+            st.step()
+    torch.cuda.synchronize()
+    status = int(st.status[0].item())
+    print(f"{w.spec.name}: {a.steps} steps, device status {status}")
+    return 0 if status == 0 else 1
+
+
+if __name__ == "__main__":
+    raise SystemExit(main())
