@@ -128,8 +128,10 @@ int make_plan(const tv_desc* d, Plan* p) {
   if (!mul_ok(splits, d->batch, &t) || !mul_ok(t, d->num_kv_heads, &t) || !mul_ok(t, row_tiles, &t) ||
       !mul_ok(t, p->tile_stride, &t))
     return TV_ERR_OVERFLOW;
+  // partial elements are bf16 when the tensor-core kernels feed a bf16 output
+  const int64_t pes = (p->pub.kernel != 0 && d->dtype == TV_BF16 && !d->out_f32) ? 2 : 4;
   int64_t o_bytes, ml_bytes;
-  if (!mul_ok(t, (int64_t)d->head_dim * 4, &o_bytes) || !mul_ok(t, 8, &ml_bytes)) return TV_ERR_OVERFLOW;
+  if (!mul_ok(t, (int64_t)d->head_dim * pes, &o_bytes) || !mul_ok(t, 8, &ml_bytes)) return TV_ERR_OVERFLOW;
   p->o_part_bytes = align_up(o_bytes, 256);
   p->ml_part_bytes = align_up(ml_bytes, 256);
   return TV_OK;
