@@ -135,13 +135,21 @@ __global__ __launch_bounds__(256) void argmax_partial_kernel(const void* __restr
                                                              int32_t* __restrict__ am_idx) {
   constexpr int ES = BF16 ? 2 : 4;
   constexpr int PER = 16 / ES;                       // elements per 16-byte load
-  constexpr int UNROLL = 4;
-  dep_wait();
-  dep_launch();
+  constexpr int UNROLL = 4;                          // words in flight per thread
   const int row = blockIdx.y, c = blockIdx.x;
   const int v0 = c * vlen;
   const int v1 = min(V, v0 + vlen);
   const int64_t rbase = (int64_t)row * V;            // element index of the row start
+  {
+    // pull this block's slice of the logits into L2 while the previous
+    // kernel runs (a prefetch does not read data before the wait)
+    const char* base = reinterpret_cast<const char*>(logits) + (rbase + v0) * ES;
+    const int64_t bytes = (int64_t)(v1 - v0) * ES;
+    for (int64_t off = (int64_t)threadIdx.x * 128; off < bytes; off += 128 * (int64_t)blockDim.x)
+      prefetch_l2(base + off);
+  }
+  dep_wait();
+  dep_launch();
   const uintptr_t addr0 = reinterpret_cast<uintptr_t>(logits) + (uintptr_t)((rbase + v0) * ES);
   int head = (int)(((16 - (addr0 & 15)) & 15) / ES);
   if ((addr0 & (ES - 1)) != 0) head = v1 - v0;       // cannot align: all scalar
@@ -163,7 +171,9 @@ __global__ __launch_bounds__(256) void argmax_partial_kernel(const void* __restr
     }
 #pragma unroll
     for (int q = 0; q < UNROLL; ++q) m[q] = (k0 + q * step < nvec) ? vec_max<BF16>(u[q]) : __int_as_float(0x7fffffff);
-    const float mb = fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));    // NaN only if all NaN
+    float mb = m[0];                                  // NaN only if all NaN
+#pragma unroll
+    for (int q = 1; q < UNROLL; ++q) mb = fmaxf(mb, m[q]);
     if (mb > bst.v || (bst.i < 0 && mb == mb)) {
       int qs = UNROLL - 1;                          // first word holding the batch maximum
 #pragma unroll
@@ -203,14 +213,17 @@ __global__ __launch_bounds__(256) void argmax_partial_kernel(const void* __restr
 // One block per sequence.  The block finishes the argmax of every node from
 // its chunk partials (four threads per node); warp 0 builds ancestors and
 // depths and walks (lane i owns nodes i and i + 32; ballots and shuffles, no
-// shared atomics); then each warp copies whole accepted K/V rows into the
+// shared atomics); then the block copies the accepted K/V rows into the
 // cache, and thread 0 advances prefix_len.
 constexpr int kCommitPages = kMaxNodes / kPageSize + 1;   // pages the k + 1 <= 64 rows can touch
+constexpr int kCommitRows = 1024;                           // rows per pass of the commit copy
 
 __global__ __launch_bounds__(256) void walk_commit_kernel(AcceptParams p) {
   __shared__ int s_par[kMaxNodes], s_draft[kMaxNodes], s_am[kMaxNodes], s_path[kMaxNodes];
   __shared__ uint64_t s_anc[kMaxNodes];
   __shared__ int s_pid[kCommitPages];
+  __shared__ const uint4* s_src[kCommitRows];
+  __shared__ uint4* s_dst[kCommitRows];
   __shared__ int s_k, s_ok;
 
   const int b = blockIdx.x;
@@ -231,6 +244,46 @@ __global__ __launch_bounds__(256) void walk_commit_kernel(AcceptParams p) {
     if (p.paged && tid >= 64 && tid < 64 + kCommitPages && P >= 0) {
       const int64_t pg = (int64_t)P / kPageSize + (tid - 64);
       s_pid[tid - 64] = pg < p.max_pages ? p.page_table[(int64_t)b * p.max_pages + pg] : -1;
+    }
+  }
+  // ancestors and depth of each node by walking parents (warp 0, lane i
+  // owns nodes i and i + 32): they need no argmax, so they overlap the
+  // argmax pass too
+  uint64_t anc[2] = {0ull, 0ull};
+  int dep[2] = {0, 0};
+  bool tree_ok[2] = {true, true};
+  __syncthreads();                                  // parents staged
+  if (valid && warp == 0) {
+#pragma unroll
+    for (int hlf = 0; hlf < 2; ++hlf) {
+      const int i = lane + 32 * hlf;
+      if (i < n) {
+        uint64_t bits = 0;
+        int d = 0, j = i;
+        bool ok = true;
+        while (true) {                              // terminates: the chain index strictly falls
+          bits |= 1ull << j;
+          const int q = s_par[j];
+          if (j == 0) {
+            ok = (q == -1);
+            break;
+          }
+          if (q < 0 || q >= j) {
+            ok = false;
+            break;
+          }
+          j = q;
+          ++d;
+        }
+        if (!ok) {
+          bits = 1ull << i;
+          d = 0;
+        }
+        anc[hlf] = bits;
+        dep[hlf] = d;
+        tree_ok[hlf] = ok;
+        s_anc[i] = bits;
+      }
     }
   }
   dep_wait();
@@ -270,41 +323,14 @@ __global__ __launch_bounds__(256) void walk_commit_kernel(AcceptParams p) {
 
   if (warp == 0) {
     const unsigned all = 0xffffffffu;
-    // ancestors and depth by walking parents; validate; match against the
-    // parent's argmax
-    uint64_t anc[2] = {0ull, 0ull};
-    int dep[2] = {0, 0};
+    // match against the parent's argmax
     bool mt[2] = {false, false}, bad = false;
 #pragma unroll
     for (int hlf = 0; hlf < 2; ++hlf) {
       const int i = lane + 32 * hlf;
       if (i < n) {
-        uint64_t bits = 0;
-        int d = 0, j = i;
-        bool ok = true;
-        while (true) {                              // terminates: the chain index strictly falls
-          bits |= 1ull << j;
-          const int q = s_par[j];
-          if (j == 0) {
-            ok = (q == -1);
-            break;
-          }
-          if (q < 0 || q >= j) {
-            ok = false;
-            break;
-          }
-          j = q;
-          ++d;
-        }
-        if (!ok) {
-          bad = true;
-          bits = 1ull << i;
-          d = 0;
-        }
-        anc[hlf] = bits;
-        dep[hlf] = d;
-        s_anc[i] = bits;
-        mt[hlf] = (i == 0) || (ok && s_draft[i] == s_am[s_par[i]]);
+        bad |= !tree_ok[hlf];
+        mt[hlf] = (i == 0) || (tree_ok[hlf] && s_draft[i] == s_am[s_par[i]]);
       }
     }
     if (__any_sync(all, bad) && lane == 0) set_status(p.status, TV_DEV_BAD_TREE);
@@ -368,54 +394,52 @@ __global__ __launch_bounds__(256) void walk_commit_kernel(AcceptParams p) {
   __syncthreads();
   if (!s_ok) return;
   const int k = s_k;
-  // copy k+1 rows x Hkv heads of K and of V: warp w takes rows w, w + 8, ...
-  // of the list (K or V, t, head), eight at a time, lane u moving 16-byte
-  // units u, u + 32, ... of each; a batch's loads are all issued before its
-  // stores (the compiler cannot prove them independent)
+  // copy k+1 rows x Hkv heads of K and of V: one thread per row writes the
+  // row's source and destination into a table, then the block moves 16-byte
+  // units (unit u of the list: row u / units_row), up to 16 loads in flight
+  // per thread, all issued before the stores
   const int64_t row_bytes = (int64_t)p.d * p.esize;
-  const int units_row = (int)(row_bytes / 16);
+  const int units_row = (int)(row_bytes / 16);      // a power of two (16 .. 128)
+  const int ushift = __ffs(units_row) - 1;
   const int kh = (k + 1) * p.Hkv, nrow = 2 * kh;
-  constexpr int RB = 8;
-  for (int r0 = warp; r0 < nrow; r0 += 8 * RB) {
-    // (kind, t, g) of row r0, then advanced 8 rows at a time
-    int kind = r0 / kh, rem = r0 - kind * kh, t = rem / p.Hkv, g = rem - t * p.Hkv;
-    const uint4* src[RB];
-    uint4* dst[RB];
-#pragma unroll
-    for (int j = 0; j < RB; ++j) {
-      src[j] = nullptr;
-      dst[j] = nullptr;
-      if (kind < 2) {
-        const int64_t pos = (int64_t)P + t;
-        int64_t drow;
-        if (p.paged) {
-          const int pid = s_pid[(P + t) / kPageSize - P / kPageSize];
-          drow = ((int64_t)pid * p.Hkv + g) * kPageSize + pos % kPageSize;
-        } else {
-          drow = ((int64_t)b * p.Hkv + g) * p.capacity + pos;
-        }
-        src[j] = reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(kind ? p.v_tree : p.k_tree) +
+  for (int c0 = 0; c0 < nrow; c0 += kCommitRows) {
+    const int cn = min(kCommitRows, nrow - c0);
+    for (int r = tid; r < cn; r += blockDim.x) {
+      const int rr = c0 + r;
+      const int kind = rr / kh, rem = rr - kind * kh, t = rem / p.Hkv, g = rem - t * p.Hkv;
+      const int64_t pos = (int64_t)P + t;
+      int64_t drow;
+      if (p.paged) {
+        const int pid = s_pid[(P + t) / kPageSize - P / kPageSize];
+        drow = ((int64_t)pid * p.Hkv + g) * kPageSize + pos % kPageSize;
+      } else {
+        drow = ((int64_t)b * p.Hkv + g) * p.capacity + pos;
+      }
+      s_src[r] = reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(kind ? p.v_tree : p.k_tree) +
                                                 ((int64_t)g * p.R + o0 + s_path[t]) * row_bytes);
-        dst[j] = reinterpret_cast<uint4*>(reinterpret_cast<char*>(kind ? p.v_cache : p.k_cache) + drow * row_bytes);
-        g += 8;                                     // next row of this warp
-        while (g >= p.Hkv) {
-          g -= p.Hkv;
-          if (++t > k) {
-            t = 0;
-            ++kind;
-          }
+      s_dst[r] = reinterpret_cast<uint4*>(reinterpret_cast<char*>(kind ? p.v_cache : p.k_cache) + drow * row_bytes);
+    }
+    __syncthreads();
+    constexpr int U = 16;
+    const int total = cn * units_row;
+    for (int base = 0; base < total; base += U * (int)blockDim.x) {
+      uint4 v[U];
+      uint4* dst[U];
+#pragma unroll
+      for (int q = 0; q < U; ++q) {
+        const int u = base + q * (int)blockDim.x + tid;
+        dst[q] = nullptr;
+        if (u < total) {
+          const int r = u >> ushift, cu = u & (units_row - 1);
+          v[q] = s_src[r][cu];
+          dst[q] = s_dst[r] + cu;
         }
       }
-    }
-    for (int u = lane; u < units_row; u += 32) {
-      uint4 v[RB];
 #pragma unroll
-      for (int j = 0; j < RB; ++j)
-        if (src[j]) v[j] = src[j][u];
-#pragma unroll
-      for (int j = 0; j < RB; ++j)
-        if (dst[j]) dst[j][u] = v[j];
+      for (int q = 0; q < U; ++q)
+        if (dst[q]) *dst[q] = v[q];
     }
+    __syncthreads();
   }
   __syncthreads();
   if (tid == 0) p.prefix_len[b] = P + k + 1;

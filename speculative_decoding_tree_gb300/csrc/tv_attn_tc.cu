@@ -164,6 +164,25 @@ tv_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (warp == 3 && lane == 0) {
+    // an idle warp warms L2 (and the TLB) for what the first steps read,
+    // while the previous kernel may still run: the sequence's lengths, the
+    // first K and V tiles of the chunk (contiguous cache) and, for the
+    // first sequence (rows start at 0), the query tile
+    const int b = blockIdx.z, g = blockIdx.y / p.splits, s = blockIdx.y % p.splits;
+    prefetch_l2(p.prefix_len + b);
+    prefetch_l2(p.node_offsets + b);
+    if (!p.paged) {
+      const int64_t row = ((int64_t)b * p.Hkv + g) * p.capacity + (int64_t)s * p.chunk;
+      if (row + BN <= (int64_t)INT_MAX)
+        for (int bx = 0; bx < D / 64; ++bx) {
+          tma_prefetch_2d(&tm_kc, bx * 64, (int)row);
+          tma_prefetch_2d(&tm_vc, bx * 64, (int)row);
+        }
+    }
+    if (b == 0)
+      for (int kb = 0; kb < D / 64; ++kb) tma_prefetch_3d(&tm_q, kb * 64, g * p.G, blockIdx.x * p.rows_per_tile / p.G);
+  }
   dep_wait();
   dep_launch();
 

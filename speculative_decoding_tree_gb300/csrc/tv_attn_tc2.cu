@@ -153,9 +153,56 @@ tv_attn_tc2_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   cluster_sync_all();                               // both CTAs' barriers exist before any remote use
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (warp == 3 && lane == 0) {
+    // an idle warp warms L2 (and the TLB) for what the first steps read,
+    // while the previous kernel may still run: the sequence's lengths,
+    // this CTA's half of the first K and V tiles of its chunk (contiguous
+    // cache) and, for the first sequence (rows start at 0), its query tile
+    const int b = blockIdx.z, g = blockIdx.y / p.splits, s = blockIdx.y % p.splits;
+    const uint32_t rank = cluster_ctarank();
+    prefetch_l2(p.prefix_len + b);
+    prefetch_l2(p.node_offsets + b);
+    if (!p.paged) {
+      const int64_t row = ((int64_t)b * p.Hkv + g) * p.capacity + (int64_t)s * p.chunk;
+      if (row + BN <= (int64_t)INT_MAX) {
+        for (int bx = 0; bx < D / 64; ++bx) tma_prefetch_2d(&tm_kc, bx * 64, (int)row + KH * (int)rank);
+        for (int bx = 0; bx < D / 128; ++bx) tma_prefetch_2d(&tm_vc, (D / 2) * (int)rank + bx * 64, (int)row);
+      }
+    }
+    if (b == 0)
+      for (int kb = 0; kb < D / 64; ++kb) tma_prefetch_3d(&tm_q, kb * 64, g * p.G, blockIdx.x * p.rows_per_tile / p.G);
+  }
   dep_wait();
   dep_launch();
 
+  // Speculative first copies, issued before the sequence's lengths are known
+  // (a dependent round trip they then overlap): the query tile when its rows
+  // start at 0 (the first sequence) and this CTA's half of the chunk's first
+  // K tile on a contiguous cache (its position needs no length).  If the
+  // chunk turns out to hold no prefix tile, slot 0's first fill is junk: the
+  // MMA issuer releases it unused and the ring starts at slot 1.  A pair with
+  // nothing to do waits for these copies before it leaves.
+  const bool spec_q = blockIdx.z == 0;
+  const bool spec_k = !p.paged && (int64_t)(blockIdx.y % p.splits) * p.chunk < p.max_prefix;
+  if (warp == 0 && lane == 0) {
+    const uint32_t rk = cluster_ctarank();
+    const int gg = blockIdx.y / p.splits, ss = blockIdx.y % p.splits;
+    if (spec_q) {
+      const uint32_t qf = map_to_cta(Q_FULL, 0);
+      if (rk == 0) mbar_expect_tx(Q_FULL, 2u * (uint32_t)p.rows_per_tile * 128u * (D / 64));
+      for (int kb = 0; kb < D / 64; ++kb)
+        tma2_load_3d(smem_u32(sQ + kb * (BM * 128)), &tm_q, qf, kb * 64, gg * p.G,
+                     (int)blockIdx.x * p.rows_per_tile / p.G);
+      if (rk != 0) mbar_arrive_cluster_relaxed(qf);
+    }
+    if (spec_k) {
+      const uint32_t fl = map_to_cta(FULL(0), 0);
+      if (rk == 0) mbar_expect_tx(FULL(0), 2 * SLOT);
+      const int64_t row = ((int64_t)blockIdx.z * p.Hkv + gg) * p.capacity + (int64_t)ss * p.chunk + KH * rk;
+      for (int bx = 0; bx < D / 64; ++bx) tma2_load_2d(smem_u32(ring + bx * (KH * 128)), &tm_kc, fl, bx * 64, (int)row);
+      if (rk != 0) mbar_arrive_cluster_relaxed(fl);
+    }
+  }
 
   // ------------------------------------------------------- work (pair-uniform)
   const uint32_t rank = cluster_ctarank();          // 0 = leader
@@ -182,20 +229,26 @@ tv_attn_tc2_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   const int tail_valid = npt > 0 ? (int)(k_end - (k_begin + (int64_t)(npt - 1) * BN)) : BN;
   const bool rows_here = m0 < nrows;                // the peer of a one-tile pair only helps
 
+  const bool junk0 = spec_k && npt == 0;           // slot 0's first fill is not this chunk's
   if (!active) {
-    // nothing for this pair: straight to teardown
+    // nothing for this pair: wait for the speculative copies (the leader's
+    // barriers count both CTAs' bytes), then teardown
+    if (warp == 0 && lane == 0 && rank == 0) {
+      if (spec_k) mbar_wait(FULL(0), 0, abort_flag, kWaitNs);
+      if (spec_q) mbar_wait(Q_FULL, 0, abort_flag, kWaitNs);
+    }
   } else if (warp == 0) {
     // ============================================================ producer
     const bool leader = rank == 0;
     const uint32_t qbytes = (uint32_t)p.rows_per_tile * 128u * (D / 64);
-    if (lane == 0) {
+    if (lane == 0 && !spec_q) {
       const uint32_t qf = map_to_cta(Q_FULL, 0);
       if (leader) mbar_expect_tx(Q_FULL, 2 * qbytes);
       for (int kb = 0; kb < D / 64; ++kb)
         tma2_load_3d(smem_u32(sQ + kb * (BM * 128)), &tm_q, qf, kb * 64, g * G, o0 + m0 / G);
       if (!leader) mbar_arrive_cluster_relaxed(qf);
     }
-    int j = 0, tail_uses = 0;
+    int j = junk0 ? 1 : 0, tail_uses = 0;
     bool ok = true;
     const int oob_row = p.paged ? (int)(p.num_pages * p.Hkv * kPageSize) : 0;
     auto page_id = [&](int tile) -> int {           // raw page id of this lane's page (lanes 0-7), or INT_MIN
@@ -227,6 +280,7 @@ tv_attn_tc2_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       for (int kind = 0; kind < 2 && ok; ++kind, ++j) {      // 0: K(t) half, 1: V(t-1) half
         const int tile = kind == 0 ? t : t - 1;
         if ((kind == 0 && t >= T) || (kind == 1 && t < 1)) { --j; continue; }
+        if (spec_k && !junk0 && t == 0 && kind == 0) continue;   // K(0) is in slot 0 already
         const bool tree = (tile == npt);
         const bool tail_fix = (kind == 1) && !tree && tile == npt - 1 && tail_valid < BN;
         const int slot = j % NS, use = j / NS;
@@ -309,6 +363,11 @@ tv_attn_tc2_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       const uint32_t q_addr = smem_u32(sQ);
       const uint32_t ring_addr = smem_u32(ring);
       int j = 0;
+      if (ok && junk0) {                            // release slot 0's speculative fill unused
+        ok = mbar_wait(FULL(0), 0, abort_flag, kWaitNs);
+        mma_commit_pair(EMPTY(0));
+        j = 1;
+      }
       for (int t = 0; t <= T && ok; ++t) {
         if (t < T) {
           const uint32_t sbuf = tmem + (uint32_t)((t & 1) * 128);

@@ -130,6 +130,13 @@ __device__ inline bool seq_rows(const int32_t* offs, int b, int R, int max_nodes
 __device__ __forceinline__ void dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// L2 prefetch of the line holding ptr: no effect on memory ordering, so a
+// kernel may issue it before dep_wait() (it only warms L2 and the TLB for
+// what the kernel reads first, while the previous kernel still runs).
+__device__ __forceinline__ void prefetch_l2(const void* ptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(ptr)));
+}
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_dep(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
                        Args&&... args) {
