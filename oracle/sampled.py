@@ -24,7 +24,7 @@ the child-by-child rule.
 
 The draw.  y_u = argmax_v (logits_u[v] / T + G_u[v]) (the Gumbel-max
 construction: the argmax of Gumbel-perturbed log-weights is a sample of the
-softmax), G = -log(-log U), U = ((x >> 8) + 0.5) * 2^-24 where x is word
+softmax), G = -log(-log U), U = ((x >> 9) + 0.5) * 2^-23 where x is word
 v % 4 of Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random
 numbers: as easy as 1, 2, 3", SC 2011) at counter (v // 4, r, offset_lo,
 offset_hi) and key (seed_lo, seed_hi); r is the tree row's index in the
@@ -67,13 +67,15 @@ def philox4x32_10(c0, c1, c2, c3, k0, k1):
 
 
 def uniforms(row, vocab, seed, offset):
-    """U[v] for v in 0..vocab-1 of tree row `row`, in (0, 1), as float64."""
+    """U[v] for v in 0..vocab-1 of tree row `row`, in (0, 1), as float64: the
+    top 23 bits of the Philox word plus one half, times 2^-23 (24 significant
+    bits, so the value is exact in float32 as well)."""
     v = np.arange(vocab, dtype=np.uint64)
     words = philox4x32_10(v >> np.uint64(2), np.uint64(row), np.uint64(offset & _MASK),
                           np.uint64((offset >> 32) & _MASK), np.uint64(seed & _MASK),
                           np.uint64((seed >> 32) & _MASK))
     x = np.choose((v & np.uint64(3)).astype(np.int64), words)
-    return ((x >> np.uint64(8)).astype(np.float64) + 0.5) * 2.0 ** -24
+    return ((x >> np.uint64(9)).astype(np.float64) + 0.5) * 2.0 ** -23
 
 
 def gumbel(row, vocab, seed, offset):

@@ -46,10 +46,11 @@ def test_philox_known_answers(golden_dir):
         assert [int(o) for o in out] == x[6:]
 
 
-def test_uniforms_in_open_interval_on_a_24_bit_grid():
+def test_uniforms_in_open_interval_exact_in_float32():
     u = sampled.uniforms(row=7, vocab=4096, seed=0x1234_5678_9abc, offset=99)
     assert (u > 0).all() and (u < 1).all()
-    assert np.allclose(u * 2 ** 24 - 0.5, np.round(u * 2 ** 24 - 0.5))
+    assert np.allclose(u * 2 ** 23 - 0.5, np.round(u * 2 ** 23 - 0.5))
+    assert (u.astype(np.float32).astype(np.float64) == u).all()
     assert 0.45 < u.mean() < 0.55
 
 
