@@ -341,6 +341,17 @@ def run_ours(args, ws, rank):
             st_.accept_commit()
         acc_calls.append(call)
     acc_us = b2b_us(acc_calls)
+    # the same calls with sampled verification (temperature 1, fresh noise per call)
+    samp_calls = []
+    for i in range(max(len(pool), n_b2b)):
+        st_, lg = pool[i % len(pool)]
+
+        def scall(st_=st_, lg=lg, i=i):
+            st_.prefix_len.copy_(st_.p0, non_blocking=True)
+            st_.logits = lg
+            st_.accept_commit_sampled(1.0, 20240601, i)
+        samp_calls.append(scall)
+    samp_us = b2b_us(samp_calls)
     for st_, lg in zip(sets, own):
         st_.logits = lg
         st_.prefix_len.copy_(st_.p0)
@@ -416,6 +427,7 @@ def run_ours(args, ws, rank):
                       "frac": round(ab["attn"] / (attn_us * 1e-6) / 1e9 / peak, 4),
                       "algorithmic_bytes": ab["attn"]},
         "accept_commit_us": round(acc_us, 2),
+        "accept_commit_sampled_us": round(samp_us, 2),
         "plan": plan,
         "device_status": status,
     }

@@ -236,6 +236,35 @@ int tree_accept_commit(const tv_desc* desc, int32_t vocab, int32_t logits_dtype,
                        int32_t* d_path, int32_t* d_tokens, void* d_workspace, size_t workspace_bytes,
                        int32_t* d_status, void* stream);
 
+/* Sampled verification (temperature > 0): the same walk, outputs and commit
+ * as tree_accept_commit, with step 1's argmax replaced by one draw per tree
+ * row from the target distribution softmax(logits[r, :] / temperature).
+ * The rule ("Speculative decoding verify batches to amortize ANE dispatch",
+ * Forge sampled-proposal bullet; "Speculative-decoding heads", What's not
+ * implemented (7)): a drafted proposal is accepted with its target
+ * probability, and on rejection the target distribution with the proposal
+ * excluded is sampled.  Drawing y_u from p_u at an accepted node u and
+ * accepting the child whose draft equals y_u is that rule (child by child,
+ * for siblings with distinct drafts); if no child matches, y_u is the
+ * correction token.  The emitted tokens therefore follow the target model's
+ * distribution whatever the drafts propose.
+ *   The draw: d_sampled[r] = argmax over v of logits[r, v] / temperature +
+ *   G(r, v), G = -log(-log U), U = ((x >> 9) + 0.5) * 2^-23 with x word v % 4
+ *   of Philox4x32-10 (Salmon et al., SC 2011) at counter (v / 4, r,
+ *   offset low, offset high) and key (seed low, seed high); NaN logits are
+ *   never drawn; computed in float32.  Pass a new offset (or seed) for every
+ *   step to draw fresh noise; the same (seed, offset) gives the same draws.
+ *   temperature must be finite and > 0 (TV_ERR_SHAPE otherwise); every other
+ *   argument, the workspace and the errors are as for tree_accept_commit, with
+ *   d_sampled in place of d_argmax. */
+int tree_accept_commit_sampled(const tv_desc* desc, int32_t vocab, int32_t logits_dtype, const void* d_logits,
+                               float temperature, uint64_t seed, uint64_t offset, const int32_t* d_draft_tokens,
+                               const int32_t* d_parents, const int32_t* d_node_offsets, const void* d_k_tree,
+                               const void* d_v_tree, void* d_k_cache, void* d_v_cache, const int32_t* d_page_table,
+                               int32_t* d_prefix_len, int32_t* d_sampled, int32_t* d_accept_len, int32_t* d_path,
+                               int32_t* d_tokens, void* d_workspace, size_t workspace_bytes, int32_t* d_status,
+                               void* stream);
+
 /* ------------------------------------- attention without a workspace */
 
 /* Size in bytes of the library's static scratch array (file-scope device

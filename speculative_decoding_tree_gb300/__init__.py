@@ -15,6 +15,7 @@ __all__ = [
     "TvDesc", "TvPlan", "TreeVerifyError", "LibraryNotBuilt", "F32", "BF16", "DEV_BITS",
     "lib", "make_desc", "tv_workspace_size", "tv_attn_plan", "tv_status_string", "tv_version",
     "tv_build_tree_mask", "tree_verify_attn", "tv_attn_partials", "tv_attn_merge", "tree_accept_commit",
+    "tree_accept_commit_sampled",
 ]
 
 F32, BF16 = 0, 1
@@ -58,6 +59,8 @@ _SIG = {
     "tv_attn_partials": [ctypes.POINTER(TvDesc)] + [_P] * 10 + [ctypes.c_size_t, _P, _P],
     "tv_attn_merge": [ctypes.POINTER(TvDesc), _P, _P, _P, _P, ctypes.c_size_t, _P, _P],
     "tree_accept_commit": [ctypes.POINTER(TvDesc), _I, _I] + [_P] * 15 + [ctypes.c_size_t, _P, _P],
+    "tree_accept_commit_sampled": [ctypes.POINTER(TvDesc), _I, _I, _P, ctypes.c_float, ctypes.c_uint64,
+                                   ctypes.c_uint64] + [_P] * 14 + [ctypes.c_size_t, _P, _P],
 }
 
 
@@ -166,3 +169,16 @@ def tree_accept_commit(desc, vocab, logits_dtype, logits, draft_tokens, parents,
                                     _ptr(prefix_len), _ptr(argmax), _ptr(accept_len), _ptr(path), _ptr(tokens),
                                     _ptr(workspace), int(workspace_bytes), _ptr(status), _stream(stream)),
            "tree_accept_commit")
+
+
+def tree_accept_commit_sampled(desc, vocab, logits_dtype, logits, temperature, seed, offset, draft_tokens, parents,
+                               node_offsets, k_tree, v_tree, k_cache, v_cache, page_table, prefix_len, sampled,
+                               accept_len, path, tokens, workspace, workspace_bytes, status, stream=None):
+    _check(lib().tree_accept_commit_sampled(ctypes.byref(desc), int(vocab), int(logits_dtype), _ptr(logits),
+                                            float(temperature), int(seed) & (2 ** 64 - 1),
+                                            int(offset) & (2 ** 64 - 1), _ptr(draft_tokens), _ptr(parents),
+                                            _ptr(node_offsets), _ptr(k_tree), _ptr(v_tree), _ptr(k_cache),
+                                            _ptr(v_cache), _ptr(page_table), _ptr(prefix_len), _ptr(sampled),
+                                            _ptr(accept_len), _ptr(path), _ptr(tokens), _ptr(workspace),
+                                            int(workspace_bytes), _ptr(status), _stream(stream)),
+           "tree_accept_commit_sampled")

@@ -208,6 +208,141 @@ __global__ __launch_bounds__(256) void argmax_partial_kernel(const void* __restr
   }
 }
 
+// ----------------------------------------------------------------- A3, sampled
+
+// Philox4x32 with 10 rounds (Salmon, Moraes, Dror, Shaw, "Parallel random
+// numbers: as easy as 1, 2, 3", SC 2011): each round multiplies words 0 and
+// 2 by the two multipliers; the new words are (hi1 ^ c1 ^ k0, lo1,
+// hi0 ^ c3 ^ k1, lo0); the key grows by the Weyl constants between rounds.
+__device__ __forceinline__ void philox4x32_10(uint32_t c[4], uint32_t k0, uint32_t k1) {
+  constexpr uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u, W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r) {
+      k0 += W0;
+      k1 += W1;
+    }
+    const uint32_t hi0 = __umulhi(M0, c[0]), lo0 = M0 * c[0];
+    const uint32_t hi1 = __umulhi(M1, c[2]), lo1 = M1 * c[2];
+    const uint32_t n0 = hi1 ^ c[1] ^ k0, n2 = hi0 ^ c[3] ^ k1;
+    c[0] = n0;
+    c[1] = lo1;
+    c[2] = n2;
+    c[3] = lo0;
+  }
+}
+
+// Gumbel noise G = -log(E), E = -log U, from a Philox word: U = ((w >> 9) +
+// 0.5) * 2^-23 and d = 1 - U are both exact in float32 and strictly inside
+// (0, 1).  The largest possible G is -log(-log(1 - 2^-24)) = 16.636...
+// E needs relative accuracy (G = -log E): for d < 1/16 it is the Mercator
+// series d + d^2/2 + ... + d^6/6 (truncation below 1e-9 relative), else the
+// hardware base-2 logarithm of U (U <= 15/16, where its absolute error is a
+// small relative one); G's base-2 logarithm needs only absolute accuracy.
+constexpr float kGumbelMax = 16.75f;
+constexpr float kLn2 = 0.69314718f;
+__device__ __forceinline__ float gumbel_of(uint32_t w) {
+  const uint32_t m = w >> 9;
+  const float d = ((float)(0x7FFFFFu - m) + 0.5f) * 0x1p-23f;     // 1 - U
+  float e;
+  if (d < 0.0625f)
+    e = d * fmaf(d, fmaf(d, fmaf(d, fmaf(d, fmaf(d, 1.f / 6.f, 0.2f), 0.25f), 1.f / 3.f), 0.5f), 1.f);
+  else
+    e = -__log2f(((float)m + 0.5f) * 0x1p-23f) * kLn2;
+  return -__log2f(e) * kLn2;
+}
+
+// Sampled verification's draw, one vocab chunk of one row per block (grid
+// (vchunks, R)): y = argmax_v (logits[v] / T + G[v]) with G from Philox at
+// counter (v / 4, row, offset) and key seed, word v % 4.  Each thread takes
+// groups of four entries in increasing order and keeps the first strictly
+// larger value, so the block reduction's smallest-index rule gives the first
+// index of the maximum; NaN never enters.  A group whose entries cannot
+// reach the thread's best even with the largest possible noise is skipped
+// without drawing its noise (the skip is exact: the bound is never met).
+template <bool BF16>
+__global__ __launch_bounds__(256) void sample_partial_kernel(const void* __restrict__ logits, int V, int vlen,
+                                                            int vchunks, float inv_t, uint32_t k0, uint32_t k1,
+                                                            uint32_t off0, uint32_t off1,
+                                                            float* __restrict__ am_val,
+                                                            int32_t* __restrict__ am_idx) {
+  constexpr int ES = BF16 ? 2 : 4;
+  const int row = blockIdx.y, c = blockIdx.x;
+  const int v0 = c * vlen;                           // a multiple of 8
+  const int v1 = min(V, v0 + vlen);
+  const int64_t rbase = (int64_t)row * V;
+  {
+    const char* base = reinterpret_cast<const char*>(logits) + (rbase + v0) * ES;
+    const int64_t bytes = (int64_t)(v1 - v0) * ES;
+    for (int64_t off = (int64_t)threadIdx.x * 128; off < bytes; off += 128 * (int64_t)blockDim.x)
+      prefetch_l2(base + off);
+  }
+  dep_wait();
+  dep_launch();
+  // four consecutive entries load as one word when the row keeps them aligned
+  const bool vec = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(logits) & (4 * ES - 1)) == 0);
+  Best bst{-INFINITY, -1};
+  for (int g = (v0 >> 2) + (int)threadIdx.x; 4 * g < v1; g += blockDim.x) {
+    float x[4];
+    const int e = 4 * g;
+    if (vec && e + 3 < v1) {
+      if (BF16) {
+        const uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(logits) + rbase + e);
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+        x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+      } else {
+        const float4 f = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(logits) + rbase + e);
+        x[0] = f.x; x[1] = f.y; x[2] = f.z; x[3] = f.w;
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) x[q] = e + q < v1 ? load_elem<BF16>(logits, rbase + e + q) : __int_as_float(0x7fffffff);
+    }
+    // no entry of the group can beat the best even with the largest noise:
+    // skip it without drawing (false for NaN)
+    bool may = bst.i < 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) may |= fmaf(x[q], inv_t, kGumbelMax) > bst.v;
+    if (!may) continue;
+    uint32_t w[4] = {(uint32_t)g, (uint32_t)row, off0, off1};
+    philox4x32_10(w, k0, k1);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (e + q >= v1) continue;
+      const float xt = x[q] * inv_t;
+      if (xt != xt) continue;                         // NaN is never drawn
+      if (bst.i >= 0) {
+        // E = -log(1 - d) >= d: when d > 1.001 e^-c (c = best - xt), G <=
+        // c - 0.001 and this entry cannot beat the best (nor can it with
+        // G's rounding); most entries leave here without a logarithm.
+        // c = -inf (xt = +inf) never prunes, c = +inf always does.
+        const float c = bst.v - xt;
+        const float d = ((float)(0x7FFFFFu - (w[q] >> 9)) + 0.5f) * 0x1p-23f;
+        if (d > 1.001f * __expf(-c)) continue;
+      }
+      take_in_order(bst, xt + gumbel_of(w[q]), e + q);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    Best o;
+    o.v = __shfl_xor_sync(0xffffffffu, bst.v, off);
+    o.i = __shfl_xor_sync(0xffffffffu, bst.i, off);
+    bst = better(bst, o);
+  }
+  __shared__ Best red[8];
+  const int w8 = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[w8] = bst;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    Best r = red[0];
+    for (int k = 1; k < (int)(blockDim.x >> 5); ++k) r = better(r, red[k]);
+    am_val[(int64_t)row * vchunks + c] = r.v;
+    am_idx[(int64_t)row * vchunks + c] = r.i;
+  }
+}
+
 // ----------------------------------------------------------------- A4 + A5
 
 // One block per sequence.  The block finishes the argmax of every node from
@@ -455,8 +590,14 @@ cudaError_t launch_tree_mask(const int32_t* parents, const int32_t* offs, uint64
 
 cudaError_t launch_accept_commit(const AcceptParams& p, cudaStream_t s) {
   dim3 grid(p.vchunks, p.R);
-  cudaError_t e = launch_dep(p.logits_bf16 ? argmax_partial_kernel<true> : argmax_partial_kernel<false>, grid,
-                             dim3(256), 0, s, p.logits, p.V, p.vchunk_len, p.vchunks, p.am_val, p.am_idx);
+  cudaError_t e;
+  if (p.sampled)
+    e = launch_dep(p.logits_bf16 ? sample_partial_kernel<true> : sample_partial_kernel<false>, grid, dim3(256), 0, s,
+                   p.logits, p.V, p.vchunk_len, p.vchunks, p.inv_temp, p.seed_lo, p.seed_hi, p.off_lo, p.off_hi,
+                   p.am_val, p.am_idx);
+  else
+    e = launch_dep(p.logits_bf16 ? argmax_partial_kernel<true> : argmax_partial_kernel<false>, grid, dim3(256), 0, s,
+                   p.logits, p.V, p.vchunk_len, p.vchunks, p.am_val, p.am_idx);
   if (e != cudaSuccess) return e;
   return launch_dep(walk_commit_kernel, dim3(p.B), dim3(256), 0, s, p);
 }

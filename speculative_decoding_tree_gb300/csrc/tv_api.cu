@@ -238,6 +238,59 @@ int launch_merge_from(const tv_desc* d, const Plan& pl, const int32_t* plen, con
   return launch_merge(m, s) == cudaSuccess ? TV_OK : TV_ERR_CUDA;
 }
 
+// tree_accept_commit and its sampled form: validation, workspace, launch.
+int accept_commit_impl(const tv_desc* desc, int32_t vocab, int32_t logits_dtype, const void* d_logits, int sampled,
+                       float temperature, uint64_t seed, uint64_t offset, const int32_t* d_draft_tokens,
+                       const int32_t* d_parents, const int32_t* d_node_offsets, const void* d_k_tree,
+                       const void* d_v_tree, void* d_k_cache, void* d_v_cache, const int32_t* d_page_table,
+                       int32_t* d_prefix_len, int32_t* d_argmax, int32_t* d_accept_len, int32_t* d_path,
+                       int32_t* d_tokens, void* d_workspace, size_t workspace_bytes, int32_t* d_status,
+                       void* stream) {
+  int rc = validate(desc);
+  if (rc) return rc;
+  if (logits_dtype != TV_F32 && logits_dtype != TV_BF16) return TV_ERR_DTYPE;
+  if (vocab < 1) return TV_ERR_SHAPE;
+  if (!d_logits || !d_draft_tokens || !d_parents || !d_node_offsets || !d_k_tree || !d_v_tree || !d_k_cache ||
+      !d_v_cache || !d_prefix_len || !d_argmax || !d_accept_len || !d_path || !d_tokens || !d_workspace ||
+      !d_status)
+    return TV_ERR_NULL;
+  if (desc->page_size == kPageSize && !d_page_table) return TV_ERR_NULL;
+  const void* all[] = {d_logits, d_draft_tokens, d_parents, d_node_offsets, d_k_tree, d_v_tree, d_k_cache,
+                       d_v_cache, d_prefix_len, d_argmax, d_accept_len, d_path, d_tokens, d_workspace, d_status};
+  for (const void* ptr : all)
+    if (!aligned16(ptr)) return TV_ERR_ALIGN;
+  if (d_page_table && !aligned16(d_page_table)) return TV_ERR_ALIGN;
+  int64_t lb;
+  if (!mul_ok(desc->total_rows, vocab, &lb) || !mul_ok(lb, 4, &lb)) return TV_ERR_OVERFLOW;
+  Plan p;
+  rc = make_plan(desc, &p);
+  if (rc) return rc;
+  int64_t off = p.o_part_bytes + p.ml_part_bytes;
+  if ((int64_t)workspace_bytes < off + accept_bytes(desc, vocab)) return TV_ERR_WORKSPACE;
+  AcceptParams a;
+  a.sampled = sampled;
+  a.inv_temp = sampled ? 1.f / temperature : 0.f;
+  a.seed_lo = (uint32_t)seed;
+  a.seed_hi = (uint32_t)(seed >> 32);
+  a.off_lo = (uint32_t)offset;
+  a.off_hi = (uint32_t)(offset >> 32);
+  a.logits = d_logits; a.logits_bf16 = logits_dtype == TV_BF16; a.V = vocab;
+  a.draft = d_draft_tokens; a.parents = d_parents; a.node_offsets = d_node_offsets;
+  a.k_tree = d_k_tree; a.v_tree = d_v_tree; a.k_cache = d_k_cache; a.v_cache = d_v_cache;
+  a.page_table = desc->page_size ? d_page_table : nullptr;
+  a.prefix_len = d_prefix_len; a.argmax = d_argmax; a.accept_len = d_accept_len;
+  a.path = d_path; a.tokens = d_tokens; a.status = d_status;
+  accept_chunks(desc->total_rows, vocab, &a.vchunks, &a.vchunk_len);
+  int64_t part = align_up((int64_t)desc->total_rows * a.vchunks * 4, 256);
+  a.am_val = reinterpret_cast<float*>(reinterpret_cast<char*>(d_workspace) + off);
+  a.am_idx = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(d_workspace) + off + part);
+  a.B = desc->batch; a.R = desc->total_rows; a.Hkv = desc->num_kv_heads; a.d = desc->head_dim;
+  a.esize = desc->dtype == TV_BF16 ? 2 : 4; a.max_nodes = desc->max_nodes; a.paged = desc->page_size != 0;
+  a.capacity = desc->capacity; a.num_pages = desc->num_pages; a.max_pages = desc->capacity / kPageSize;
+  cudaError_t e = launch_accept_commit(a, as_stream(stream));
+  return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace tv
 
@@ -376,43 +429,23 @@ int tree_accept_commit(const tv_desc* desc, int32_t vocab, int32_t logits_dtype,
                        const int32_t* d_page_table, int32_t* d_prefix_len, int32_t* d_argmax,
                        int32_t* d_accept_len, int32_t* d_path, int32_t* d_tokens, void* d_workspace,
                        size_t workspace_bytes, int32_t* d_status, void* stream) {
-  int rc = validate(desc);
-  if (rc) return rc;
-  if (logits_dtype != TV_F32 && logits_dtype != TV_BF16) return TV_ERR_DTYPE;
-  if (vocab < 1) return TV_ERR_SHAPE;
-  if (!d_logits || !d_draft_tokens || !d_parents || !d_node_offsets || !d_k_tree || !d_v_tree || !d_k_cache ||
-      !d_v_cache || !d_prefix_len || !d_argmax || !d_accept_len || !d_path || !d_tokens || !d_workspace ||
-      !d_status)
-    return TV_ERR_NULL;
-  if (desc->page_size == kPageSize && !d_page_table) return TV_ERR_NULL;
-  const void* all[] = {d_logits, d_draft_tokens, d_parents, d_node_offsets, d_k_tree, d_v_tree, d_k_cache,
-                       d_v_cache, d_prefix_len, d_argmax, d_accept_len, d_path, d_tokens, d_workspace, d_status};
-  for (const void* ptr : all)
-    if (!aligned16(ptr)) return TV_ERR_ALIGN;
-  if (d_page_table && !aligned16(d_page_table)) return TV_ERR_ALIGN;
-  int64_t lb;
-  if (!mul_ok(desc->total_rows, vocab, &lb) || !mul_ok(lb, 4, &lb)) return TV_ERR_OVERFLOW;
-  Plan p;
-  rc = make_plan(desc, &p);
-  if (rc) return rc;
-  int64_t off = p.o_part_bytes + p.ml_part_bytes;
-  if ((int64_t)workspace_bytes < off + accept_bytes(desc, vocab)) return TV_ERR_WORKSPACE;
-  AcceptParams a;
-  a.logits = d_logits; a.logits_bf16 = logits_dtype == TV_BF16; a.V = vocab;
-  a.draft = d_draft_tokens; a.parents = d_parents; a.node_offsets = d_node_offsets;
-  a.k_tree = d_k_tree; a.v_tree = d_v_tree; a.k_cache = d_k_cache; a.v_cache = d_v_cache;
-  a.page_table = desc->page_size ? d_page_table : nullptr;
-  a.prefix_len = d_prefix_len; a.argmax = d_argmax; a.accept_len = d_accept_len;
-  a.path = d_path; a.tokens = d_tokens; a.status = d_status;
-  accept_chunks(desc->total_rows, vocab, &a.vchunks, &a.vchunk_len);
-  int64_t part = align_up((int64_t)desc->total_rows * a.vchunks * 4, 256);
-  a.am_val = reinterpret_cast<float*>(reinterpret_cast<char*>(d_workspace) + off);
-  a.am_idx = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(d_workspace) + off + part);
-  a.B = desc->batch; a.R = desc->total_rows; a.Hkv = desc->num_kv_heads; a.d = desc->head_dim;
-  a.esize = desc->dtype == TV_BF16 ? 2 : 4; a.max_nodes = desc->max_nodes; a.paged = desc->page_size != 0;
-  a.capacity = desc->capacity; a.num_pages = desc->num_pages; a.max_pages = desc->capacity / kPageSize;
-  cudaError_t e = launch_accept_commit(a, as_stream(stream));
-  return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+  return accept_commit_impl(desc, vocab, logits_dtype, d_logits, 0, 0.f, 0, 0, d_draft_tokens, d_parents,
+                            d_node_offsets, d_k_tree, d_v_tree, d_k_cache, d_v_cache, d_page_table, d_prefix_len,
+                            d_argmax, d_accept_len, d_path, d_tokens, d_workspace, workspace_bytes, d_status, stream);
+}
+
+int tree_accept_commit_sampled(const tv_desc* desc, int32_t vocab, int32_t logits_dtype, const void* d_logits,
+                               float temperature, uint64_t seed, uint64_t offset, const int32_t* d_draft_tokens,
+                               const int32_t* d_parents, const int32_t* d_node_offsets, const void* d_k_tree,
+                               const void* d_v_tree, void* d_k_cache, void* d_v_cache, const int32_t* d_page_table,
+                               int32_t* d_prefix_len, int32_t* d_sampled, int32_t* d_accept_len, int32_t* d_path,
+                               int32_t* d_tokens, void* d_workspace, size_t workspace_bytes, int32_t* d_status,
+                               void* stream) {
+  if (!(temperature > 0.f) || !std::isfinite(temperature) || !std::isfinite(1.f / temperature)) return TV_ERR_SHAPE;
+  return accept_commit_impl(desc, vocab, logits_dtype, d_logits, 1, temperature, seed, offset, d_draft_tokens,
+                            d_parents, d_node_offsets, d_k_tree, d_v_tree, d_k_cache, d_v_cache, d_page_table,
+                            d_prefix_len, d_sampled, d_accept_len, d_path, d_tokens, d_workspace, workspace_bytes,
+                            d_status, stream);
 }
 
 }  // extern "C"

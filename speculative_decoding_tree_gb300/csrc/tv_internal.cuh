@@ -185,6 +185,9 @@ struct AcceptParams {
   int64_t capacity, num_pages, max_pages;
   int vchunks;               // vocab chunks per row in the argmax pass
   int vchunk_len;            // elements per chunk (multiple of 8)
+  int sampled;               // draw per row (Gumbel-max) instead of the argmax
+  float inv_temp;            // 1 / temperature (sampled)
+  uint32_t seed_lo, seed_hi, off_lo, off_hi;   // Philox key and counter words 2, 3 (sampled)
 };
 
 cudaError_t launch_accept_commit(const AcceptParams& p, cudaStream_t s);

@@ -9,8 +9,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (BF16, F32, make_desc, tree_accept_commit, tree_verify_attn, tv_attn_merge, tv_attn_partials,
-               tv_build_tree_mask, tv_workspace_size)
+from . import (BF16, F32, make_desc, tree_accept_commit, tree_accept_commit_sampled, tree_verify_attn, tv_attn_merge,
+               tv_attn_partials, tv_build_tree_mask, tv_workspace_size)
 
 _DT = {torch.float32: F32, torch.bfloat16: BF16}
 
@@ -77,6 +77,15 @@ class DeviceStep:
                            self.page_table, self.prefix_len, self.argmax, self.accept_len, self.path,
                            self.tokens, self.workspace, self.ws_bytes, self.status, stream)
 
+    def accept_commit_sampled(self, temperature, seed, offset, stream=None):
+        """Sampled verification: one draw per tree row (written to self.argmax),
+        then the same walk and commit."""
+        tree_accept_commit_sampled(self.desc, self.vocab, self.logits_dtype, self.logits, temperature, seed, offset,
+                                   self.draft, self.parents, self.node_offsets, self.k_tree, self.v_tree,
+                                   self.k_cache, self.v_cache, self.page_table, self.prefix_len, self.argmax,
+                                   self.accept_len, self.path, self.tokens, self.workspace, self.ws_bytes,
+                                   self.status, stream)
+
     def step(self, stream=None):
         """One verify step: mask, attention, accept + commit."""
         self.mask(stream)
@@ -103,6 +112,8 @@ def main(argv=None):
     ap.add_argument("--config", type=int, default=4, help="workload 1..5")
     ap.add_argument("--steps", type=int, default=3)
     ap.add_argument("--attn-only", action="store_true", help="mask and attention only")
+    ap.add_argument("--sampled", type=float, default=0.0,
+                    help="temperature > 0: sampled verification (tree_accept_commit_sampled)")
     a = ap.parse_args(argv)
     _build.build()
     w = wl.make_workload(wl.CONFIGS[a.config], canary=0.0,
@@ -114,6 +125,10 @@ def main(argv=None):
         if a.attn_only:
             st.mask()
             st.attn()
+        elif a.sampled > 0:
+            st.mask()
+            st.attn()
+            st.accept_commit_sampled(a.sampled, 1234, _)
         else:
             st.step()
     torch.cuda.synchronize()

@@ -105,3 +105,15 @@ def test_workspace_and_plan(L):
     assert tv.tv_attn_plan(_desc(max_nodes=2, total_rows=2))["kernel"] == 0   # 8 rows per KV head
     g3 = tv.tv_attn_plan(_desc(num_q_heads=24))                               # G = 3: 126-row tiles
     assert g3["kernel"] == 2 and g3["rows_per_tile"] == 126
+
+
+def test_sampled_rejects_bad_temperature(L):
+    d = _desc()
+    fake = 1 << 20
+    args = [fake] * 14
+    for t in (0.0, -1.0, float("nan"), float("inf"), 1e-45):
+        rc = L.tree_accept_commit_sampled(ctypes.byref(d), 1000, 1, fake, t, 1, 2, *args, 1 << 30, fake, None)
+        assert rc == -6, t
+    # otherwise the same host checks as the greedy call
+    assert L.tree_accept_commit_sampled(ctypes.byref(d), 1000, 5, fake, 1.0, 1, 2, *args, 1 << 30, fake, None) == -2
+    assert L.tree_accept_commit_sampled(ctypes.byref(d), 1000, 1, fake, 1.0, 1, 2, *args, 64, fake, None) == -10
