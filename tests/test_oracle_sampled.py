@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 
 from oracle import sampled
-from oracle.tree_verify import accept, argmax_row
+from oracle.tree_verify import accept, argmax_row, argmax_rows
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 
@@ -128,3 +128,25 @@ def test_second_token_follows_the_accepted_nodes_distribution():
     p_ex[2] = 0
     p_ex /= p_ex.sum()
     assert first_rej[2] == 0 and chi2_ok(first_rej, p_ex)
+
+
+def test_whole_step_is_lossless_per_sequence():
+    # the step function itself (draws, walk over a batch of trees, commit):
+    # over many offsets the first token each sequence emits follows that
+    # sequence's root distribution, and the cache grows by the accepted rows
+    from speculative_decoding_tree_gb300 import workloads as wl
+    spec = wl.CONFIGS[5].replace(batch=2, hq=4, hkv=2, d=32, prefix=(3, 9), vocab=12,
+                                 tree="random:5,5,3", seed=31)
+    w = wl.make_workload(spec, argmax_fn=argmax_rows)
+    t = 1.3
+    roots = [w.seq_rows(b)[0] for b in range(w.batch)]
+    logits = np.asarray(w.logits.float(), dtype=np.float64)
+    first = np.zeros((w.batch, spec.vocab))
+    p_before = np.asarray(w.prefix_len, dtype=np.int64).copy()
+    for off in range(2500):
+        st = sampled.verify_step_sampled(w, t, seed=2024, offset=off, samples=[(roots[0], 0)])
+        for b, (k, path, tokens) in enumerate(st["accepted"]):
+            first[b, tokens[0]] += 1
+            assert int(st["prefix_len"][b]) == p_before[b] + k + 1
+    for b in range(w.batch):
+        assert chi2_ok(first[b], softmax(logits[roots[b]], t)), (b, first[b])
