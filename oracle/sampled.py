@@ -89,15 +89,26 @@ def perturbed(logits_row, temperature, row, seed, offset):
     return x / float(temperature) + gumbel(row, x.shape[0], seed, offset)
 
 
-def sample_row(logits_row, temperature, row, seed, offset):
-    """One draw from softmax(logits_row / T): the first index of the largest
-    perturbed value among the non-NaN entries (0 for an all-NaN row)."""
+def draw_with_margin(logits_row, temperature, row, seed, offset):
+    """(draw, margin) of one row from one evaluation of the perturbed values.
+    The draw is the first index of the largest perturbed value among the
+    non-NaN entries (0 for an all-NaN row); the margin is the gap between the
+    largest and the second-largest of them (inf with fewer than two): a draw
+    computed in lower precision agrees with this one when the gap is well
+    above that precision's rounding."""
     s = perturbed(logits_row, temperature, row, seed, offset)
     ok = ~np.isnan(s)
     if not ok.any():
-        return 0
+        return 0, float("inf")
     idx = np.flatnonzero(ok)
-    return int(idx[np.argmax(s[idx])])
+    y = int(idx[np.argmax(s[idx])])
+    v = np.sort(s[idx])
+    return y, (float(v[-1] - v[-2]) if v.shape[0] > 1 else float("inf"))
+
+
+def sample_row(logits_row, temperature, row, seed, offset):
+    """One draw from softmax(logits_row / T)."""
+    return draw_with_margin(logits_row, temperature, row, seed, offset)[0]
 
 
 def sample_rows(logits, temperature, seed, offset):
@@ -107,12 +118,8 @@ def sample_rows(logits, temperature, seed, offset):
 
 
 def sample_margin(logits_row, temperature, row, seed, offset):
-    """Gap between the largest and second-largest perturbed values of a row:
-    a draw computed in lower precision agrees with this one when the gap is
-    well above that precision's rounding."""
-    s = perturbed(logits_row, temperature, row, seed, offset)
-    s = np.sort(s[~np.isnan(s)])
-    return float(s[-1] - s[-2]) if s.shape[0] > 1 else float("inf")
+    """Gap between the largest and second-largest perturbed values of a row."""
+    return draw_with_margin(logits_row, temperature, row, seed, offset)[1]
 
 
 def verify_step_sampled(w, temperature, seed, offset, samples=None):
