@@ -112,7 +112,7 @@ def expand_tree(logits_of, root_token, k, n_max, width, max_depth, token_map=Non
         while len(expand) < width and len(tokens) < n_max and pool:
             pool.sort(key=lambda c: (-c[0], c[1]))
             c = pool.pop(0)
-            gaps.append(c[0] - pool[0][0] if pool else float("inf"))
+            gaps.append(float("inf") if not pool else 0.0 if c[0] == pool[0][0] else c[0] - pool[0][0])
             tokens.append(c[3])
             parents.append(c[2])
             depths.append(c[4])
