@@ -1,7 +1,8 @@
 """Tree-verify step of tree speculative decoding on GB300 (sm_103a).
 
 A thin ctypes binding over libtreeverify.so, whose C ABI is declared in
-include/tree_verify.h.  Every function here only marshals arguments (torch
+include/tree_verify.h (the verify step) and include/tree_expand.h (dynamic
+draft-tree expansion).  Every function here only marshals arguments (torch
 tensors or raw device addresses, a stream) and raises on a non-zero status;
 all work happens in the library's CUDA kernels.  There is no CPU fallback:
 calling into a library that was not built raises ``LibraryNotBuilt``.
@@ -15,11 +16,13 @@ __all__ = [
     "TvDesc", "TvPlan", "TreeVerifyError", "LibraryNotBuilt", "F32", "BF16", "DEV_BITS",
     "lib", "make_desc", "tv_workspace_size", "tv_attn_plan", "tv_status_string", "tv_version",
     "tv_build_tree_mask", "tree_verify_attn", "tv_attn_partials", "tv_attn_merge", "tree_accept_commit",
-    "tree_accept_commit_sampled",
+    "tree_accept_commit_sampled", "TvExpandDesc", "make_expand_desc", "tv_expand_workspace_size",
+    "tv_expand_steps", "tv_tree_expand_step",
 ]
 
 F32, BF16 = 0, 1
-DEV_BITS = {1: "BAD_TREE", 2: "BAD_OFFSETS", 4: "BAD_PREFIX", 8: "BAD_PAGE", 16: "CAPACITY", 32: "TIMEOUT"}
+DEV_BITS = {1: "BAD_TREE", 2: "BAD_OFFSETS", 4: "BAD_PREFIX", 8: "BAD_PAGE", 16: "CAPACITY", 32: "TIMEOUT",
+            64: "BAD_LOGITS", 128: "BAD_STEP"}
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtreeverify.so")
 
 
@@ -48,6 +51,11 @@ class TvPlan(ctypes.Structure):
                 ("kernel", "num_splits", "chunk", "row_tiles", "rows_per_tile", "grid_ctas")]
 
 
+class TvExpandDesc(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("batch", "vocab", "top_k", "width", "max_nodes", "max_depth", "logits_dtype")]
+
+
 _LIB = None
 _P = ctypes.c_void_p
 _I = ctypes.c_int32
@@ -61,6 +69,10 @@ _SIG = {
     "tree_accept_commit": [ctypes.POINTER(TvDesc), _I, _I] + [_P] * 15 + [ctypes.c_size_t, _P, _P],
     "tree_accept_commit_sampled": [ctypes.POINTER(TvDesc), _I, _I, _P, ctypes.c_float, ctypes.c_uint64,
                                    ctypes.c_uint64] + [_P] * 14 + [ctypes.c_size_t, _P, _P],
+    "tv_expand_workspace_size": [ctypes.POINTER(TvExpandDesc), ctypes.POINTER(ctypes.c_size_t)],
+    "tv_expand_steps": [ctypes.POINTER(TvExpandDesc), ctypes.POINTER(ctypes.c_int32)],
+    "tv_tree_expand_step": [ctypes.POINTER(TvExpandDesc), _I, _P, ctypes.c_int64] + [_P] * 9
+                           + [ctypes.c_size_t, _P, _P],
 }
 
 
@@ -182,3 +194,27 @@ def tree_accept_commit_sampled(desc, vocab, logits_dtype, logits, temperature, s
                                             _ptr(accept_len), _ptr(path), _ptr(tokens), _ptr(workspace),
                                             int(workspace_bytes), _ptr(status), _stream(stream)),
            "tree_accept_commit_sampled")
+
+
+def make_expand_desc(*, batch, vocab, top_k, width, max_nodes, max_depth, logits_dtype) -> TvExpandDesc:
+    return TvExpandDesc(batch, vocab, top_k, width, max_nodes, max_depth, logits_dtype)
+
+
+def tv_expand_workspace_size(desc: TvExpandDesc) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().tv_expand_workspace_size(ctypes.byref(desc), ctypes.byref(n)), "tv_expand_workspace_size")
+    return n.value
+
+
+def tv_expand_steps(desc: TvExpandDesc) -> int:
+    n = ctypes.c_int32(0)
+    _check(lib().tv_expand_steps(ctypes.byref(desc), ctypes.byref(n)), "tv_expand_steps")
+    return n.value
+
+
+def tv_tree_expand_step(desc, step, logits, seq_stride, root_tokens, token_map, tokens, parents, depths, cum,
+                        n_nodes, expand_count, workspace, workspace_bytes, status, stream=None):
+    _check(lib().tv_tree_expand_step(ctypes.byref(desc), int(step), _ptr(logits), int(seq_stride),
+                                     _ptr(root_tokens), _ptr(token_map), _ptr(tokens), _ptr(parents), _ptr(depths),
+                                     _ptr(cum), _ptr(n_nodes), _ptr(expand_count), _ptr(workspace),
+                                     int(workspace_bytes), _ptr(status), _stream(stream)), "tv_tree_expand_step")

@@ -33,7 +33,8 @@ def sources():
 
 def _deps():
     hdr = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
-    hdr.append(os.path.join(ROOT, "include", "tree_verify.h"))
+    inc = os.path.join(ROOT, "include")
+    hdr += [os.path.join(inc, f) for f in os.listdir(inc) if f.endswith(".h")]
     return max(os.path.getmtime(h) for h in hdr)
 
 

@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cstring>
 
+#include "tree_expand.h"
 #include "tv_internal.cuh"
 
 namespace tv {
@@ -16,6 +17,8 @@ bool add_ok(int64_t a, int64_t b, int64_t* out) { return !__builtin_add_overflow
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
 
 int num_sms() {
   static int cached = 0;
@@ -30,6 +33,8 @@ int num_sms() {
   }
   return n;
 }
+
+namespace {
 
 // Checks shared by every entry point.  Order follows the pages' validation
 // list: dtype, head_dim, zero heads before the GQA modulo, shapes, overflow
@@ -321,6 +326,8 @@ const char* tv_status_string(int code) {
     case TV_DEV_BAD_PAGE: return "device: page id out of range";
     case TV_DEV_CAPACITY: return "device: accepted rows do not fit the cache";
     case TV_DEV_TIMEOUT: return "device: bounded wait ran out";
+    case TV_DEV_BAD_LOGITS: return "device: +inf draft logit (node not expanded)";
+    case TV_DEV_BAD_STEP: return "device: expansion step out of order";
     default: return "unknown";
   }
 }

@@ -153,6 +153,9 @@ cudaError_t launch_dep(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
+// SMs of the current device (cached; a default when no device answers).
+int num_sms();
+
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_attn_simt(const AttnParams& p, int dtype, cudaStream_t s);
 cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t s);

@@ -1,5 +1,6 @@
 """Device-resident buffers for one verify workload and the C-ABI calls of a
-verify step, in stream order: tree mask, attention, accept + commit.
+verify step, in stream order: tree mask, attention, accept + commit; and the
+same for one dynamic draft-tree expansion (DeviceExpand).
 
 Used by the benchmark, the GPU tests and the smoke check.  It only moves a
 workload's tensors to the GPU, allocates the outputs and workspace with
@@ -9,8 +10,9 @@ from __future__ import annotations
 
 import torch
 
-from . import (BF16, F32, make_desc, tree_accept_commit, tree_accept_commit_sampled, tree_verify_attn, tv_attn_merge,
-               tv_attn_partials, tv_build_tree_mask, tv_workspace_size)
+from . import (BF16, F32, make_desc, make_expand_desc, tree_accept_commit, tree_accept_commit_sampled,
+               tree_verify_attn, tv_attn_merge, tv_attn_partials, tv_build_tree_mask, tv_expand_steps,
+               tv_expand_workspace_size, tv_tree_expand_step, tv_workspace_size)
 
 _DT = {torch.float32: F32, torch.bfloat16: BF16}
 
@@ -97,6 +99,47 @@ class DeviceStep:
         the plan has one key chunk), argmax, walk + commit."""
         from . import tv_attn_plan
         return 4 + (1 if tv_attn_plan(self.desc)["num_splits"] > 1 else 0)
+
+
+class DeviceExpand:
+    """Device buffers of one expansion workload (workloads.ExpandSpec): the
+    synthetic drafter's logits of every step (resident), the roots, the tree
+    outputs and the workspace; step(s) is one tv_tree_expand_step call."""
+
+    def __init__(self, spec, device="cuda", rows=None, token_map=None, steps=None):
+        from . import workloads as wl
+        dev = torch.device(device)
+        self.spec = spec
+        dt = {"f32": F32, "bf16": BF16}[spec.dtype]
+        self.desc = make_expand_desc(batch=spec.batch, vocab=spec.vocab, top_k=spec.top_k, width=spec.width,
+                                     max_nodes=spec.max_nodes, max_depth=spec.max_depth, logits_dtype=dt)
+        self.steps = tv_expand_steps(self.desc) if steps is None else int(steps)
+        if rows is None:
+            rows = [wl.draft_rows(spec, s) for s in range(self.steps)]
+        self.rows = [r.to(dev).contiguous() for r in rows]
+        self.roots = wl.root_tokens(spec).to(dev)
+        self.token_map = None if token_map is None else token_map.to(dev).to(torch.int32).contiguous()
+        B, N = spec.batch, spec.max_nodes
+        self.tokens = torch.zeros(B, N, dtype=torch.int32, device=dev)
+        self.parents = torch.zeros(B, N, dtype=torch.int32, device=dev)
+        self.depths = torch.zeros(B, N, dtype=torch.int32, device=dev)
+        self.cum = torch.zeros(B, N, dtype=torch.float64, device=dev)
+        self.n_nodes = torch.zeros(B, dtype=torch.int32, device=dev)
+        self.expand_count = torch.zeros(B, dtype=torch.int32, device=dev)
+        self.status = torch.zeros(4, dtype=torch.int32, device=dev)
+        self.ws_bytes = tv_expand_workspace_size(self.desc)
+        self.workspace = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
+
+    def step(self, s, stream=None):
+        x = self.rows[s]
+        tv_tree_expand_step(self.desc, s, x, x.shape[1] * x.shape[2], self.roots, self.token_map, self.tokens,
+                            self.parents, self.depths, self.cum, self.n_nodes, self.expand_count, self.workspace,
+                            self.ws_bytes, self.status, stream)
+
+    def run(self, stream=None):
+        """Every step, in order (two kernel launches each)."""
+        for s in range(self.steps):
+            self.step(s, stream)
 
 
 def main(argv=None):

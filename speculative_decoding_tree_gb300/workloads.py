@@ -353,3 +353,55 @@ def small_variant(n: int, **kw) -> Spec:
     }[n]
     defaults.update(kw)
     return s.replace(**defaults)
+
+
+# ----------------------------------------------------------------------------
+# dynamic draft-tree expansion: the drafter's logits, one seeded block per step
+# ----------------------------------------------------------------------------
+
+@dataclass(frozen=True)
+class ExpandSpec:
+    """An expansion workload ("ADR-037 — EAGLE-3 with dynamic tree port",
+    phase row E4a and §4 Phase E4: top-K per expanded node, a budget of 64
+    nodes; the verify workloads' EAGLE-2 tree is top-8 to depth 6)."""
+    name: str
+    batch: int
+    vocab: int
+    top_k: int
+    width: int
+    max_nodes: int
+    max_depth: int
+    dtype: str                 # draft logits: "f32" or "bf16"
+    logit_std: float
+    seed: int
+
+    def replace(self, **kw) -> "ExpandSpec":
+        return dataclasses.replace(self, **kw)
+
+
+EXPAND_CONFIGS = {
+    # one tree: top-8, 8 nodes per drafter call, 64 nodes, depth <= 6, Qwen-size vocabulary
+    "eagle2": ExpandSpec("expand-eagle2-bf16-v151936-k8-w8-n64", 1, 151936, 8, 8, 64, 6, "bf16", 3.0, 2001),
+    # the batched verify workload's 16 sequences, Llama-size vocabulary, depth <= 8
+    "batched": ExpandSpec("expand-batched-bf16-v128256-k8-w8-n64-b16", 16, 128256, 8, 8, 64, 8, "bf16", 3.0,
+                          2002),
+}
+
+
+def draft_rows(spec: ExpandSpec, step: int) -> torch.Tensor:
+    """The synthetic drafter's logits for one expansion step: [B, R, V] with
+    R = 1 at step 0 (the roots) and W after (row j = the j-th node the
+    previous step moved into tree b), N(0, logit_std) drawn in fp32 from
+    torch.Generator('cpu').manual_seed(seed * 1000003 + step) and cast to the
+    spec's dtype.  A real drafter's row depends on the node's token path; the
+    expansion never looks at that, only at the row it is given."""
+    R = 1 if step == 0 else spec.width
+    g = torch.Generator("cpu").manual_seed(spec.seed * 1000003 + step)
+    x = torch.randn(spec.batch, R, spec.vocab, generator=g) * spec.logit_std
+    return x.to(_torch_dtype(spec.dtype))
+
+
+def root_tokens(spec: ExpandSpec) -> torch.Tensor:
+    """[B] int32 root (anchor) tokens, uniform over the vocabulary."""
+    g = torch.Generator("cpu").manual_seed(spec.seed * 1000003 - 1)
+    return torch.randint(0, spec.vocab, (spec.batch,), generator=g, dtype=torch.int64).to(torch.int32)

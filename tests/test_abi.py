@@ -1,5 +1,5 @@
-"""The C-ABI library loads, exports every symbol include/tree_verify.h
-declares, and rejects bad arguments on the host before any launch.  CPU only:
+"""The C-ABI library loads, exports every symbol the headers under include/
+declare, and rejects bad arguments on the host before any launch.  CPU only:
 no call here reaches a kernel."""
 import ctypes
 import os
@@ -11,7 +11,7 @@ import speculative_decoding_tree_gb300 as tv
 from speculative_decoding_tree_gb300 import _build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "tree_verify.h")
+INCLUDE = os.path.join(ROOT, "include")
 
 
 @pytest.fixture(scope="module")
@@ -21,7 +21,11 @@ def L():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    text = ""
+    for f in sorted(os.listdir(INCLUDE)):
+        if f.endswith(".h"):
+            with open(os.path.join(INCLUDE, f)) as fh:
+                text += fh.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"^\s*(?:const\s+)?(?:int|size_t|char\s*\*|void)\s*\**\s*(\w+)\s*\(", text,
                                  flags=re.M)))
@@ -29,7 +33,8 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(L):
     names = declared_functions()
-    assert {"tree_verify_attn", "tree_accept_commit", "tv_build_tree_mask", "tv_workspace_size"} <= set(names)
+    assert {"tree_verify_attn", "tree_accept_commit", "tv_build_tree_mask", "tv_workspace_size",
+            "tv_tree_expand_step", "tv_expand_steps", "tv_expand_workspace_size"} <= set(names)
     for n in names:
         assert hasattr(L, n), n
 
@@ -37,7 +42,7 @@ def test_exports_every_declared_symbol(L):
 def test_codes_have_names(L):
     for code in range(0, -13, -1):
         assert tv.tv_status_string(code) != "unknown"
-    for bit in (1, 2, 4, 8, 16, 32):
+    for bit in (1, 2, 4, 8, 16, 32, 64, 128):
         assert tv.tv_status_string(bit).startswith("device:")
     assert tv.tv_status_string(12345) == "unknown"
     assert "sm_103a" in tv.tv_version()
@@ -117,3 +122,43 @@ def test_sampled_rejects_bad_temperature(L):
     # otherwise the same host checks as the greedy call
     assert L.tree_accept_commit_sampled(ctypes.byref(d), 1000, 5, fake, 1.0, 1, 2, *args, 1 << 30, fake, None) == -2
     assert L.tree_accept_commit_sampled(ctypes.byref(d), 1000, 1, fake, 1.0, 1, 2, *args, 64, fake, None) == -10
+
+
+def _xdesc(**kw):
+    base = dict(batch=1, vocab=151936, top_k=8, width=8, max_nodes=64, max_depth=6, logits_dtype=tv.BF16)
+    base.update(kw)
+    return tv.make_expand_desc(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(logits_dtype=3), -2), (dict(batch=0), -6), (dict(batch=4096), -6), (dict(vocab=0), -6),
+    (dict(top_k=0), -6), (dict(top_k=17), -6), (dict(width=0), -6), (dict(width=17), -6),
+    (dict(max_nodes=0), -6), (dict(max_nodes=65), -6), (dict(max_depth=0), -6),
+])
+def test_expand_descriptor_validation(L, kw, code):
+    d = _xdesc(**kw)
+    n = ctypes.c_size_t(0)
+    assert L.tv_expand_workspace_size(ctypes.byref(d), ctypes.byref(n)) == code
+    fake = 1 << 20
+    assert L.tv_tree_expand_step(ctypes.byref(d), 0, fake, 1 << 20, *([fake] * 9), 1 << 30, fake, None) == code
+
+
+def test_expand_host_checks(L):
+    d = _xdesc()
+    fake = 1 << 20
+    ptrs = [fake] * 9
+    ws = tv.tv_expand_workspace_size(d)
+    step = lambda s, stride, p, wsb: L.tv_tree_expand_step(ctypes.byref(d), s, p[0], stride, *p[1:], wsb, fake, None)
+    assert L.tv_tree_expand_step(None, 0, fake, 151936, *ptrs, ws, fake, None) == -1
+    bad = [fake] + [None] + ptrs[1:]                                   # no root tokens at step 0
+    assert step(0, 151936, bad, ws) == -1
+    assert step(1, 151936, bad, ws) == -6                               # (a later step may pass no roots)
+    assert step(0, 151935, [fake] * 10, ws) == -6                      # rows of one tree overlap the next
+    assert step(1, 151936, [fake] * 10, ws) == -6                      # a later step reads W rows per tree
+    assert step(-1, 151936, [fake] * 10, ws) == -6
+    assert step(0, 151936, [fake + 8] + [fake] * 9, ws) == -11
+    assert step(0, 151936, [fake] * 10, ws - 1) == -10
+    assert tv.tv_expand_steps(d) == 8                                  # 1 + 8 + 8 + ... + 7 nodes
+    assert tv.tv_expand_steps(_xdesc(width=1)) == 63
+    assert tv.tv_expand_steps(_xdesc(top_k=1, width=4)) == 63          # a chain: one node per step
+    assert tv.tv_expand_steps(_xdesc(max_nodes=1)) == 1
