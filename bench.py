@@ -218,6 +218,46 @@ def algorithmic_bytes(w):
 
 # ---------------------------------------------------------------- our arm
 
+def expansion_timing(cap_stream, reps=5, trees_per_graph=8):
+    """Dynamic draft-tree expansion: every step of one whole expansion
+    (two launches per step), `trees_per_graph` expansions back to back in one
+    CUDA graph, events around the graph; per tree = total / trees.  The
+    drafter's rows of every step are resident (a real drafter writes each
+    step's rows just before the step, so they would be in L2 as well)."""
+    from speculative_decoding_tree_gb300.runner import DeviceExpand
+    out = {}
+    for key in ("eagle2", "batched"):
+        spec = wl.EXPAND_CONFIGS[key]
+        dx = DeviceExpand(spec)
+        dx.run()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap_stream):
+            for _ in range(trees_per_graph):
+                dx.run()
+        g.replay()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda._sleep(2_000_000)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3 / trees_per_graph)
+        tree_us = statistics.median(ts)
+        logit_bytes = sum(r.numel() * r.element_size() for r in dx.rows)
+        out[key] = {"workload": spec.name, "batch": spec.batch, "vocab": spec.vocab, "top_k": spec.top_k,
+                    "width": spec.width, "max_nodes": spec.max_nodes, "steps": dx.steps,
+                    "expansion_us": round(tree_us, 2), "step_us": round(tree_us / dx.steps, 2),
+                    "launches": 2 * dx.steps, "draft_logit_bytes": logit_bytes,
+                    "gbs": round(logit_bytes / (tree_us * 1e-6) / 1e9, 1),
+                    "nodes": int(dx.n_nodes.sum().item()), "device_status": int(dx.status[0].item())}
+        del dx, g
+    return out
+
+
 def run_ours(args, ws, rank):
     import numpy as np  # noqa: F401
     from speculative_decoding_tree_gb300 import _build
@@ -356,6 +396,7 @@ def run_ours(args, ws, rank):
         st_.logits = lg
         st_.prefix_len.copy_(st_.p0)
     del pool
+    expansion = expansion_timing(cap_stream)
     timing_mode = ("back-to-back launches of each call in one CUDA graph over the rotating input sets, "
                    "programmatic dependent launch between them; per launch = events around the graph / launches")
     clocks = sampler.stop() if sampler else None
@@ -428,8 +469,9 @@ def run_ours(args, ws, rank):
                       "algorithmic_bytes": ab["attn"]},
         "accept_commit_us": round(acc_us, 2),
         "accept_commit_sampled_us": round(samp_us, 2),
+        "expansion": expansion,
         "plan": plan,
-        "device_status": status,
+        "device_status": status | max(e["device_status"] for e in expansion.values()),
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(spec, args.cpu_seconds)

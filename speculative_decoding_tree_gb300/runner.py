@@ -157,8 +157,18 @@ def main(argv=None):
     ap.add_argument("--attn-only", action="store_true", help="mask and attention only")
     ap.add_argument("--sampled", type=float, default=0.0,
                     help="temperature > 0: sampled verification (tree_accept_commit_sampled)")
+    ap.add_argument("--expand", default="", help="run a dynamic-expansion workload instead (eagle2, batched)")
     a = ap.parse_args(argv)
     _build.build()
+    if a.expand:
+        dx = DeviceExpand(wl.EXPAND_CONFIGS[a.expand])
+        for _ in range(a.steps):
+            dx.run()
+        torch.cuda.synchronize()
+        status = int(dx.status[0].item())
+        print(f"{dx.spec.name}: {a.steps} expansions of {dx.steps} steps, {int(dx.n_nodes.sum())} nodes, "
+              f"device status {status}")
+        return 0 if status == 0 else 1
     w = wl.make_workload(wl.CONFIGS[a.config], canary=0.0,
                          argmax_fn=lambda x: torch.argmax(x.float(), dim=1))   # plants the draft tokens
     st = DeviceStep(w)
