@@ -22,9 +22,9 @@
  *   values in increasing token order (the smaller token wins ties), compared
  *   as the raw logits (never a rounded or clamped copy); NaN is never chosen.
  *   Log-probability of token v: logit[v] - log sum_u exp(logit[u]) over the
- *   non-NaN entries (computed with the row maximum subtracted; the sum of
- *   exponentials in float32 per thread and float64 across threads; the
- *   log and the subtraction in float64).
+ *   non-NaN entries (computed with the maximum subtracted; the sum of
+ *   exponentials in float32 within a warp and float64 across warps and
+ *   vocabulary chunks; the log and the subtraction in float64).
  *
  * The drafter is the caller's: between two steps it computes the draft
  * logits of the nodes the previous step moved into the tree.
@@ -103,6 +103,9 @@ int tv_expand_steps(const tv_expand_desc* desc, int32_t* steps);
  *                  of d_logits the drafter must fill for tree b (0 once the
  *                  tree is complete); they are nodes
  *                  [d_n_nodes - d_expand_count, d_n_nodes).
+ *
+ * Enqueues two kernels; step 0 also enqueues a memset of 4 * B * W bytes of
+ * the workspace (per-row counters that later steps find at zero again).
  *
  * Errors: TV_ERR_NULL, TV_ERR_DTYPE, TV_ERR_SHAPE (a descriptor field, step
  * or seq_stride out of range), TV_ERR_OVERFLOW, TV_ERR_WORKSPACE,

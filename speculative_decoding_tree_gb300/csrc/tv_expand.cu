@@ -1,11 +1,11 @@
 // Dynamic draft-tree expansion ("ADR-037 — EAGLE-3 with dynamic tree port",
 // phase rows E4a and E4b.10a, §4 Phase E4), one step per call:
 //
-//   draft_topk_kernel   grid (vocabulary chunks, expanded rows): each CTA
-//                       reads one chunk of one row of draft logits once and
+//   draft_topk_kernel   grid (vocabulary chunks, expanded rows): each
+//                       CTA reads one chunk of one row of draft logits and
 //                       leaves its top-K entries (largest first, smaller
-//                       index on ties) and its log-sum-exp partial (running
-//                       maximum, sum of exponentials).
+//                       index on ties) and its log-sum-exp partial (maximum,
+//                       sum of exponentials).
 //   expand_step_kernel  one CTA per tree: merges the chunks of each expanded
 //                       row into its top-K children with float64 cumulative
 //                       log-probabilities, ranks them together with the
@@ -29,20 +29,26 @@ namespace {
 constexpr int kXK = 16;          // largest top_k
 constexpr int kXW = 16;          // largest width
 constexpr int kXN = 64;          // largest max_nodes
-constexpr int kXChunks = 64;     // largest number of vocabulary chunks per row
 constexpr int kXThreads = 256;
 constexpr int kXMaxBatch = 4095; // rows of one step (batch x width) fit a grid's y dimension
 constexpr int32_t kXMagic = 0x54455850;
 constexpr float kLog2e = 1.4426950408889634f;
 
-// One tree's state between steps (in the workspace).
+// One tree's state between steps (in the workspace).  Cumulative
+// log-probabilities are float pairs (hi + lo, see DF below).
 struct XState {
   int32_t magic, step, n_nodes, pool_n;
   int32_t gen, exp_count, done, pad;
   int32_t exp_node[kXW];                 // nodes the next step expands (row j = exp_node[j])
-  double pool_cum[kXN];                  // pending candidates, sorted: best first
+  float pool_hi[kXN], pool_lo[kXN];      // pending candidates, sorted: best first
   int32_t pool_parent[kXN], pool_token[kXN], pool_depth[kXN], pool_order[kXN];
+  float node_hi[kXN], node_lo[kXN];      // the tree's nodes
+  int32_t node_depth[kXN];
 };
+
+
+static_assert(sizeof(XState) % 16 == 0, "the state is copied in 16-byte units");
+static_assert(kXN == 64, "");
 
 // An entry of a top-K list: logit and vocabulary index (i < 0: empty).
 struct Ent {
@@ -59,14 +65,78 @@ __device__ __forceinline__ bool ent_before(Ent a, Ent b) {
   return a.i < b.i;
 }
 
-__device__ __forceinline__ Ent warp_first(Ent e) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    Ent o{__shfl_xor_sync(0xffffffffu, e.v, off), __shfl_xor_sync(0xffffffffu, e.i, off)};
-    if (ent_before(o, e)) e = o;
-  }
-  return e;
+// The first entry of the warp in the order of ent_before, by two warp
+// reductions: the largest value (as an order-preserving integer key; an
+// empty entry has key 0, below every value), then the smallest index among
+// the lanes holding it.
+__device__ __forceinline__ uint32_t val_key(float v) {
+  uint32_t b = __float_as_uint(v);
+  if (b == 0x80000000u) b = 0;                             // -0 orders as +0
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
+
+__device__ __forceinline__ float key_val(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+__device__ __forceinline__ Ent warp_first(Ent e) {
+  const uint32_t vk = e.i < 0 ? 0u : val_key(e.v);
+  const uint32_t best = __reduce_max_sync(0xffffffffu, vk);
+  const uint32_t bi = __reduce_min_sync(0xffffffffu, (e.i >= 0 && vk == best) ? (uint32_t)e.i : 0xffffffffu);
+  return best == 0u ? Ent{-INFINITY, -1} : Ent{key_val(best), (int)bi};
+}
+
+// Double-float arithmetic.  A value is hi + lo with |lo| <= ulp(hi) / 2
+// (about 48 significant bits), computed with float32 error-free
+// transformations (Knuth's two-sum, Dekker's fast two-sum).  Float64
+// arithmetic on this part has a dependent latency of about 30-70 ns per
+// operation (against about 2 ns in float32), and the step is a chain of
+// dependent operations, so the cumulative log-probabilities are carried as
+// float pairs and converted to float64 only when written out.
+struct DF {
+  float hi, lo;
+};
+
+__device__ __forceinline__ DF df_norm(float s, float e) {   // |e| small against s
+  if (!(fabsf(s) < INFINITY)) return DF{s, 0.f};
+  const float h = __fadd_rn(s, e);
+  return DF{h, __fsub_rn(e, __fsub_rn(h, s))};
+}
+
+__device__ __forceinline__ DF df_add(DF a, DF b) {
+  const float s = __fadd_rn(a.hi, b.hi);
+  if (!(fabsf(s) < INFINITY)) return DF{s, 0.f};
+  const float bb = __fsub_rn(s, a.hi);
+  const float e = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, bb)), __fsub_rn(b.hi, bb));
+  return df_norm(s, __fadd_rn(e, __fadd_rn(a.lo, b.lo)));
+}
+
+__device__ __forceinline__ DF df_neg(DF a) { return DF{-a.hi, -a.lo}; }
+
+// a * f for a float f >= 0 (the product's rounding error recovered by an fma)
+__device__ __forceinline__ DF df_mulf(DF a, float f) {
+  const float p = __fmul_rn(a.hi, f);
+  if (!(fabsf(p) < INFINITY)) return DF{p, 0.f};
+  const float e = __fmaf_rn(a.hi, f, -p);
+  return df_norm(p, __fmaf_rn(a.lo, f, e));
+}
+
+// log(S) for 1 <= S < 2^30: S = m * 2^e with m in [1, 2), e * ln2 with ln2
+// split so that e * ln2_hi is exact, plus logf(m) (at most 1 ulp of a value
+// below 0.7): within about 1e-7.
+__device__ __forceinline__ DF df_log_ge1(DF S) {
+  int e;
+  const float m2 = frexpf(S.hi, &e);                      // S.hi = m2 * 2^e, m2 in [0.5, 1)
+  const float m = 2.f * m2;
+  const float le = (float)(e - 1);
+  const DF a = df_add(DF{le * 0.693145751953125f, 0.f}, DF{le * 1.428606765330187e-06f, 0.f});
+  // log(S.hi + S.lo) = log(S.hi) + S.lo / S.hi to first order
+  return df_add(a, DF{logf(m), __fdiv_rn(S.lo, S.hi)});
+}
+
+// An integer with the order of the double-float value (hi, then lo): the
+// pool compares these instead of floating-point values.
+__device__ __forceinline__ uint64_t df_key(DF a) { return ((uint64_t)val_key(a.hi) << 32) | val_key(a.lo); }
 
 // A thread's KT best entries, sorted.  Entries arrive in increasing index
 // order, so a new entry equal to the last one held loses the tie.
@@ -102,140 +172,263 @@ __device__ __forceinline__ float load_logit(const void* base, int64_t e) {
   return reinterpret_cast<const float*>(base)[e];
 }
 
-// (m, s) pairs of a log-sum-exp: s = sum of exp(x - m); m = -inf means empty.
-__device__ __forceinline__ void lse_combine(float& m, double& s, float m2, double s2) {
-  const float M = fmaxf(m, m2);
-  double r = 0.0;
-  if (m > -INFINITY) r += s * (double)exp2f((m - M) * kLog2e);
-  if (m2 > -INFINITY) r += s2 * (double)exp2f((m2 - M) * kLog2e);
-  m = M;
-  s = r;
+// The top-K pass: CTAs of kXTopkThreads threads, each reading one chunk of
+// one row in tiles of kXTopkThreads * kXTile entries (thread t holds kXTile
+// entries of a tile, in increasing index order).
+constexpr int kXTopkThreads = 512;
+constexpr int kXTile = 16;
+constexpr int kXTileElems = kXTopkThreads * kXTile;  // 8192
+constexpr int kXRowEntries = 512;                    // chunks x K per row (the step stages them in shared memory)
+constexpr int kXCand = 1024;                         // candidates a CTA ranks directly
+
+// Loads the thread's entries of one tile (NaN where the chunk ends), with
+// their indices.  vec: 16-byte loads (rows 16-byte aligned).
+template <bool BF16>
+__device__ __forceinline__ void load_tile(const void* logits, int64_t rbase, int t0, int v1, int vec, float x[kXTile],
+                                          int ix[kXTile]) {
+  constexpr int ES = BF16 ? 2 : 4;
+  constexpr int VE = 16 / ES;
+  if (vec) {
+#pragma unroll
+    for (int g = 0; g < kXTile / VE; ++g) {
+      const int e = t0 + (g * kXTopkThreads + (int)threadIdx.x) * VE;
+      if (e + VE <= v1) {
+        const uint4 u = *reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(logits) + (rbase + e) * ES);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        if (BF16) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[q]));
+            x[g * VE + 2 * q] = f.x;
+            x[g * VE + 2 * q + 1] = f.y;
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) x[g * VE + q] = __uint_as_float(w[q]);
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < VE; ++q) x[g * VE + q] = e + q < v1 ? load_logit<BF16>(logits, rbase + e + q) : __int_as_float(0x7fffffff);
+      }
+#pragma unroll
+      for (int q = 0; q < VE; ++q) ix[g * VE + q] = e + q;
+    }
+  } else {
+#pragma unroll
+    for (int g = 0; g < kXTile; ++g) {
+      const int e = t0 + g * kXTopkThreads + (int)threadIdx.x;
+      x[g] = e < v1 ? load_logit<BF16>(logits, rbase + e) : __int_as_float(0x7fffffff);
+      ix[g] = e;
+    }
+  }
 }
 
-// grid (vchunks, B * R).  Row j of tree b starts at element b * seq_stride +
-// j * V.  Leaves, per (row, chunk): the chunk's top-K in pv / pi (stride
-// kXK), its maximum in pm (+inf when the chunk holds +inf) and its sum of
-// exponentials in ps.
+// grid (vchunks, B * R), kXTopkThreads threads.  Row j of tree b starts at
+// element b * seq_stride + j * V; CTA c reads entries [c * vlen, (c+1) * vlen).
+//
+// Pass 1: each thread's first maximum; the CTA's maximum M, and a threshold T
+// no larger than the CTA's K-th largest entry: the smallest of the warps'
+// maxima (16 warps, K <= 16, so 16 distinct entries are >= T).  Pass 2: the
+// sum of exp(x - M), and every entry >= T as a candidate; the candidates'
+// first K by rank are the CTA's top-K.  (More than kXCand candidates, e.g. a
+// chunk of equal logits: per-thread sorted lists and K rounds of warp
+// merges instead.)  Leaves, per (row, chunk): the top-K in pv / pi at
+// ((row * vchunks + chunk) * K, -1 indices after the valid entries), the
+// maximum in pm (+inf when the chunk holds +inf) and the sum of
+// exponentials in ps (a double-float: float32 per thread, pairs above).
 template <bool BF16, int KT>
-__global__ __launch_bounds__(kXThreads) void draft_topk_kernel(const void* __restrict__ logits, int64_t seq_stride,
-                                                               int V, int R, int vlen, int vchunks, int K, int vec,
-                                                               float* __restrict__ pv, int32_t* __restrict__ pi,
-                                                               float* __restrict__ pm, double* __restrict__ ps) {
+__global__ __launch_bounds__(kXTopkThreads) void draft_topk_kernel(const void* __restrict__ logits, int64_t seq_stride,
+                                                                   int V, int R, int vlen, int vchunks, int K, int vec,
+                                                                   float* __restrict__ pv, int32_t* __restrict__ pi,
+                                                                   float* __restrict__ pm, float2* __restrict__ ps) {
   constexpr int ES = BF16 ? 2 : 4;
+  constexpr int NW = kXTopkThreads / 32;
   const int row = blockIdx.y, c = blockIdx.x;
   const int b = row / R, j = row - b * R;
   const int64_t rbase = (int64_t)b * seq_stride + (int64_t)j * V;
   const int v0 = c * vlen;                       // a multiple of 8
   const int v1 = min(V, v0 + vlen);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   {
     const char* base = reinterpret_cast<const char*>(logits) + (rbase + v0) * ES;
     const int64_t bytes = (int64_t)(v1 - v0) * ES;
     for (int64_t off = (int64_t)threadIdx.x * 128; off < bytes; off += 128 * (int64_t)blockDim.x)
       prefetch_l2(base + off);
   }
+  __shared__ float s_wmax[NW];
+  __shared__ int s_wi[NW];
+  __shared__ float s_sum[NW], s_sum_lo[NW];
+  __shared__ int s_cnt;
+  __shared__ float cv[kXCand];
+  __shared__ int ci[kXCand];
+  __shared__ Ent wtop[NW][KT];
+  if (threadIdx.x == 0) s_cnt = 0;
   dep_wait();
   dep_launch();
 
-  TopList<KT> L;
-  L.init();
-  float m = -INFINITY, s = 0.f;
+  // pass 1: the thread's first maximum (NaN and +inf excluded); the first
+  // tile stays in registers for pass 2
+  float x[kXTile];
+  int ix[kXTile];
+  float tmax = -INFINITY;
+  int tidx = -1;
   bool bad = false;
-  auto take = [&](float x, int idx) {
-    if (x != x) return;                          // NaN: never a child, not in the sum
-    if (x == INFINITY) {
-      bad = true;
-      return;
-    }
-    if (x > m) {
-      s = s * exp2f((m - x) * kLog2e) + 1.f;
-      m = x;
-    } else if (x > -INFINITY) {
-      s += exp2f((x - m) * kLog2e);
-    }
-    L.push(x, idx);
-  };
-  if (vec) {
-    constexpr int VE = 16 / ES;                  // elements per 16-byte load
-    for (int e = v0 + (int)threadIdx.x * VE; e < v1; e += (int)blockDim.x * VE) {
-      if (e + VE <= v1) {
-        const uint4 u = *reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(logits) + (rbase + e) * ES);
-        float x[VE];
-        if (BF16) {
-          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  const bool one_tile = v1 - v0 <= kXTileElems;
+  for (int t0 = v0; t0 < v1; t0 += kXTileElems) {
+    load_tile<BF16>(logits, rbase, t0, v1, vec, x, ix);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[q]));
-            x[2 * q] = f.x;
-            x[2 * q + 1] = f.y;
-          }
-        } else {
-          x[0] = __uint_as_float(u.x);
-          x[1] = __uint_as_float(u.y);
-          x[2] = __uint_as_float(u.z);
-          x[3] = __uint_as_float(u.w);
+    for (int k = 0; k < kXTile; ++k) {
+      const float xv = x[k];
+      if (xv != xv) continue;
+      if (xv == INFINITY) {
+        bad = true;
+        continue;
+      }
+      if (tidx < 0 || xv > tmax) {
+        tmax = xv;
+        tidx = ix[k];
+      }
+    }
+  }
+  const Ent wm = warp_first(Ent{tmax, tidx});
+  if (lane == 0) {
+    s_wmax[warp] = wm.i >= 0 ? wm.v : -INFINITY;
+    s_wi[warp] = wm.i;
+  }
+  const int any_bad = __syncthreads_or(bad);
+  float M = -INFINITY, T = INFINITY;
+  bool no_thr = false;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    M = fmaxf(M, s_wmax[w]);
+    T = fminf(T, s_wmax[w]);
+    no_thr |= s_wi[w] < 0;
+  }
+  if (no_thr) T = -INFINITY;                     // a warp without entries: every entry is a candidate
+
+  // pass 2: sum of exponentials and candidates
+  float s = 0.f;
+  auto scan = [&](void) {
+#pragma unroll
+    for (int k = 0; k < kXTile; ++k) {
+      const float xv = x[k];
+      if (!(xv < INFINITY)) continue;            // NaN, +inf
+      if (xv > -INFINITY) s += exp2f((xv - M) * kLog2e);
+    }
+    // candidates (>= T), appended with one shared atomic per warp and entry slot
+#pragma unroll
+    for (int k = 0; k < kXTile; ++k) {
+      const float xv = x[k];
+      const bool cand = xv < INFINITY && xv >= T;  // not NaN, not +inf
+      const uint32_t m = __ballot_sync(0xffffffffu, cand);
+      if (m == 0u) continue;
+      int base = 0;
+      if (lane == __ffs(m) - 1) base = atomicAdd(&s_cnt, __popc(m));
+      base = __shfl_sync(0xffffffffu, base, __ffs(m) - 1);
+      if (cand) {
+        const int pos = base + __popc(m & ((1u << lane) - 1u));
+        if (pos < kXCand) {
+          cv[pos] = xv;
+          ci[pos] = ix[k];
         }
+      }
+    }
+  };
+  if (one_tile) {
+    scan();                                      // the tile pass 1 left in registers
+  } else {
+    for (int t0 = v0; t0 < v1; t0 += kXTileElems) {
+      load_tile<BF16>(logits, rbase, t0, v1, vec, x, ix);
+      scan();
+    }
+  }
+  DF sw{s, 0.f};
 #pragma unroll
-        for (int q = 0; q < VE; ++q) take(x[q], e + q);
-      } else {
-        for (int q = 0; e + q < v1; ++q) take(load_logit<BF16>(logits, rbase + e + q), e + q);
+  for (int off = 16; off > 0; off >>= 1)
+    sw = df_add(sw, DF{__shfl_xor_sync(0xffffffffu, sw.hi, off), __shfl_xor_sync(0xffffffffu, sw.lo, off)});
+  if (lane == 0) {
+    s_sum[warp] = sw.hi;
+    s_sum_lo[warp] = sw.lo;
+  }
+  __syncthreads();
+  const int64_t slot = (int64_t)row * vchunks + c;
+  const int n = s_cnt;
+  float* ov = pv + slot * K;
+  int32_t* oi = pi + slot * K;
+  if (n <= kXCand) {
+    // warp 0: K rounds, each taking the first remaining candidate
+    if (warp == 0) {
+      int r = 0;
+      for (; r < K; ++r) {
+        Ent mine{-INFINITY, -1};
+        int mu = -1;
+        for (int u = lane; u < n; u += 32) {
+          const Ent c2{cv[u], ci[u]};
+          if (ent_before(c2, mine)) {
+            mine = c2;
+            mu = u;
+          }
+        }
+        const Ent best = warp_first(mine);
+        if (best.i < 0) break;                     // fewer than K candidates
+        if (mine.i == best.i) ci[mu] = -1;         // taken
+        if (lane == 0) {
+          ov[r] = best.v;
+          oi[r] = best.i;
+        }
+        __syncwarp();
+      }
+      for (int r2 = r + lane; r2 < K; r2 += 32) {
+        ov[r2] = -INFINITY;
+        oi[r2] = -1;
       }
     }
   } else {
-    for (int e = v0 + (int)threadIdx.x; e < v1; e += blockDim.x) take(load_logit<BF16>(logits, rbase + e), e);
-  }
-
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  constexpr int NW = kXThreads / 32;
-  __shared__ Ent wtop[NW][KT];
-  __shared__ float red_m[NW];
-  __shared__ double red_s[NW];
-
-  // log-sum-exp partial
-  double sd = s;
+    // many equal entries: per-thread sorted lists, then K rounds of merges
+    TopList<KT> L;
+    L.init();
+    for (int t0 = v0; t0 < v1; t0 += kXTileElems) {
+      load_tile<BF16>(logits, rbase, t0, v1, vec, x, ix);
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
-    const double s2 = __shfl_xor_sync(0xffffffffu, sd, off);
-    lse_combine(m, sd, m2, s2);
-  }
-  if (lane == 0) {
-    red_m[warp] = m;
-    red_s[warp] = sd;
-  }
-  // top-K of each warp: K rounds of the warp's first head
-  for (int r = 0; r < K; ++r) {
-    const Ent best = warp_first(L.e[0]);
-    if (best.i >= 0 && L.e[0].i == best.i) L.pop();
-    if (lane == 0) wtop[warp][r] = best;
-  }
-  const int any_bad = __syncthreads_or(bad);
-  const int64_t slot = (int64_t)row * vchunks + c;
-  if (warp == 0) {
-    int pos = 0;
+      for (int k = 0; k < kXTile; ++k)
+        if (x[k] < INFINITY) L.push(x[k], ix[k]);
+    }
     for (int r = 0; r < K; ++r) {
-      const Ent h = (lane < NW && pos < K) ? wtop[lane][pos] : Ent{-INFINITY, -1};
-      const Ent best = warp_first(h);
-      if (lane < NW && h.i >= 0 && h.i == best.i) ++pos;
-      if (lane == 0) {
-        pv[slot * kXK + r] = best.v;
-        pi[slot * kXK + r] = best.i;
+      const Ent best = warp_first(L.e[0]);
+      if (best.i >= 0 && L.e[0].i == best.i) L.pop();
+      if (lane == 0) wtop[warp][r] = best;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int pos = 0;
+      for (int r = 0; r < K; ++r) {
+        const Ent h = (lane < NW && pos < K) ? wtop[lane][pos] : Ent{-INFINITY, -1};
+        const Ent best = warp_first(h);
+        if (lane < NW && h.i >= 0 && h.i == best.i) ++pos;
+        if (lane == 0) {
+          ov[r] = best.v;
+          oi[r] = best.i;
+        }
       }
     }
+  }
+  if (warp == 0) {
+    DF S = lane < NW ? DF{s_sum[lane], s_sum_lo[lane]} : DF{0.f, 0.f};
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+      S = df_add(S, DF{__shfl_xor_sync(0xffffffffu, S.hi, off), __shfl_xor_sync(0xffffffffu, S.lo, off)});
     if (lane == 0) {
-      float M = red_m[0];
-      double S = red_s[0];
-      for (int w = 1; w < NW; ++w) lse_combine(M, S, red_m[w], red_s[w]);
       pm[slot] = any_bad ? INFINITY : M;
-      ps[slot] = S;
+      ps[slot] = make_float2(S.hi, S.lo);
     }
   }
 }
 
 struct XParams {
-  const float* pv;
-  const int32_t* pi;
-  const float* pm;
-  const double* ps;
+  const float* pv;           // [B * R, vchunks, K] each chunk's top-K logits, largest first
+  const int32_t* pi;         // their vocabulary indices (-1 after the valid entries)
+  const float* pm;           // [B * R, vchunks] chunk maximum (+inf: the chunk holds +inf)
+  const float2* ps;          // [B * R, vchunks] sum of exp(x - chunk maximum), double-float
   const int32_t* root_tokens;
   const int32_t* token_map;
   int32_t* tokens;
@@ -251,16 +444,16 @@ struct XParams {
 
 // a precedes b in the pool order: larger cumulative log-probability first,
 // equal values to the candidate generated first (orders are unique).
-__device__ __forceinline__ bool cand_before(double ca, int oa, double cb, int ob) {
-  return ca > cb || (ca == cb && oa < ob);
+__device__ __forceinline__ bool cand_before(uint64_t ka, int oa, uint64_t kb, int ob) {
+  return ka > kb || (ka == kb && oa < ob);
 }
 
-// Entries of the sorted run (cum[0..n), order[0..n)) that precede (c, o).
-__device__ __forceinline__ int count_before(const double* cum, const int* order, int n, double c, int o) {
+// Entries of the sorted run (key[0..n), order[0..n)) that precede (k, o).
+__device__ __forceinline__ int count_before(const uint64_t* key, const int* order, int n, uint64_t k, int o) {
   int lo = 0, hi = n;
   while (lo < hi) {
     const int mid = (lo + hi) >> 1;
-    if (cand_before(cum[mid], order[mid], c, o)) lo = mid + 1;
+    if (cand_before(key[mid], order[mid], k, o)) lo = mid + 1;
     else hi = mid;
   }
   return lo;
@@ -278,15 +471,25 @@ __global__ __launch_bounds__(kXThreads) void expand_step_kernel(XParams p) {
 
   __shared__ int s_ok, s_n, s_pool_n, s_gen, s_exp_count, s_done;
   __shared__ int s_exp_node[kXW], s_exp_depth[kXW], s_count[kXW];
-  __shared__ double s_exp_cum[kXW];
-  __shared__ double c_cum[kXW * kXK];            // new candidates, row j at [j * K, j * K + count_j)
+  __shared__ DF s_exp_cum[kXW];
+  __shared__ DF c_cum[kXW * kXK];                // new candidates, row j at [j * K, j * K + count_j)
+  __shared__ uint64_t c_key[kXW * kXK];
   __shared__ int c_parent[kXW * kXK], c_token[kXW * kXK], c_depth[kXW * kXK], c_order[kXW * kXK];
-  __shared__ double q_cum[kXN];                   // pending pool (sorted)
+  __shared__ DF q_cum[kXN];                      // pending pool (sorted)
+  __shared__ uint64_t q_key[kXN];
   __shared__ int q_parent[kXN], q_token[kXN], q_depth[kXN], q_order[kXN];
+  __shared__ __align__(16) XState s_st;
 
-  dep_wait();
-  dep_launch();
-
+  // The state step - 1 left.  That grid completed before the top-K grid of
+  // this step passed its own dependency wait, which comes before the moment
+  // this grid may start, so it is read here, before this grid's wait, from
+  // L2 (the top-K grid does not touch it).
+  if (p.step > 0) {
+    const uint4* src = reinterpret_cast<const uint4*>(st);
+    uint4* dst = reinterpret_cast<uint4*>(&s_st);
+    for (int i = tid; i < (int)(sizeof(XState) / 16); i += blockDim.x) dst[i] = __ldcg(src + i);
+  }
+  __syncthreads();
   if (tid == 0) {
     if (p.step == 0) {
       s_ok = 1;
@@ -296,14 +499,17 @@ __global__ __launch_bounds__(kXThreads) void expand_step_kernel(XParams p) {
       s_exp_count = 1;
       s_done = 0;
       s_exp_node[0] = 0;
+      s_st.node_hi[0] = 0.f;
+      s_st.node_lo[0] = 0.f;
+      s_st.node_depth[0] = 0;
     } else {
       // the state must be the one step - 1 left for this descriptor
       // (anything else, e.g. a workspace of another expansion, is refused)
-      const int n = st->n_nodes, pn = st->pool_n, ec = st->exp_count;
-      int ok = st->magic == kXMagic && st->step == p.step - 1 && n >= 1 && n <= p.N && pn >= 0 &&
+      const int n = s_st.n_nodes, pn = s_st.pool_n, ec = s_st.exp_count;
+      int ok = s_st.magic == kXMagic && s_st.step == p.step - 1 && n >= 1 && n <= p.N && pn >= 0 &&
                pn <= p.N - n && ec >= 0 && ec <= p.R && ec < n;
       for (int j = 0; ok && j < ec; ++j) {
-        const int u = st->exp_node[j];
+        const int u = s_st.exp_node[j];
         ok = u >= 1 && u < n;
         s_exp_node[j] = u;
       }
@@ -313,14 +519,35 @@ __global__ __launch_bounds__(kXThreads) void expand_step_kernel(XParams p) {
       } else {
         s_n = n;
         s_pool_n = pn;
-        s_gen = st->gen;
+        s_gen = s_st.gen;
         s_exp_count = ec;
-        s_done = st->done;
+        s_done = s_st.done;
       }
     }
   }
   __syncthreads();
-  if (!s_ok) return;
+  if (!s_ok) {
+    dep_wait();
+    dep_launch();
+    return;
+  }
+  const int E = s_exp_count, K = p.K, P = s_pool_n;
+  if (tid < kXW) s_count[tid] = 0;
+  if (tid < E) {
+    const int u = s_exp_node[tid];
+    s_exp_depth[tid] = s_st.node_depth[u];
+    s_exp_cum[tid] = DF{s_st.node_hi[u], s_st.node_lo[u]};
+  }
+  if (tid < P) {
+    q_cum[tid] = DF{s_st.pool_hi[tid], s_st.pool_lo[tid]};
+    q_key[tid] = df_key(q_cum[tid]);
+    q_parent[tid] = s_st.pool_parent[tid];
+    q_token[tid] = s_st.pool_token[tid];
+    q_depth[tid] = s_st.pool_depth[tid];
+    q_order[tid] = s_st.pool_order[tid];
+  }
+  dep_wait();
+  dep_launch();
   if (p.step == 0) {
     for (int i = tid; i < p.N; i += blockDim.x) {
       tok[i] = i ? -1 : p.root_tokens[b];
@@ -337,35 +564,29 @@ __global__ __launch_bounds__(kXThreads) void expand_step_kernel(XParams p) {
     }
     return;
   }
-  const int E = s_exp_count, K = p.K, P = s_pool_n;
-  if (tid < kXW) s_count[tid] = 0;
-  if (tid < E) {
-    const int u = s_exp_node[tid];
-    s_exp_depth[tid] = p.step == 0 ? 0 : dep[u];
-    s_exp_cum[tid] = p.step == 0 ? 0.0 : cum[u];
-  }
-  if (tid < P) {
-    q_cum[tid] = st->pool_cum[tid];
-    q_parent[tid] = st->pool_parent[tid];
-    q_token[tid] = st->pool_token[tid];
-    q_depth[tid] = st->pool_depth[tid];
-    q_order[tid] = st->pool_order[tid];
-  }
   __syncthreads();
 
-  // children of each expanded row: warp j % NW merges row j's chunks
-  const int vc = p.vchunks;
+  // children of each expanded row (warp j % NW): the row's log-sum-exp from
+  // its chunks, and its top-K by K rounds over the heads of the chunks'
+  // sorted lists (staged in shared memory with one round of loads)
+  __shared__ float w_v[NW][kXRowEntries];
+  __shared__ int w_i[NW][kXRowEntries];
+  const int vc = p.vchunks, nE = vc * K;
   for (int j = warp; j < E; j += NW) {
     if (s_exp_depth[j] >= p.max_depth) continue;   // at the depth limit: no children
     const int64_t row = (int64_t)b * p.R + j;
-    const float* pm = p.pm + row * vc;
-    const double* ps = p.ps + row * vc;
+    const float* rv = p.pv + row * nE;
+    const int32_t* ri = p.pi + row * nE;
+    for (int t = lane; t < nE; t += 32) {
+      w_v[warp][t] = rv[t];
+      w_i[warp][t] = ri[t];
+    }
     float M = -INFINITY;
     bool bad = false;
-    for (int c = lane; c < vc; c += 32) {
-      const float mc = pm[c];
-      if (mc == INFINITY) bad = true;
-      else M = fmaxf(M, mc);
+    for (int cc = lane; cc < vc; cc += 32) {
+      const float mc = p.pm[row * vc + cc];
+      bad |= mc == INFINITY;
+      if (mc != INFINITY) M = fmaxf(M, mc);
     }
     if (__any_sync(0xffffffffu, bad)) {
       if (lane == 0) set_status(p.status, TV_DEV_BAD_LOGITS);
@@ -373,41 +594,55 @@ __global__ __launch_bounds__(kXThreads) void expand_step_kernel(XParams p) {
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    double S = 0.0;
-    for (int c = lane; c < vc; c += 32) {
-      const float mc = pm[c];
-      if (mc > -INFINITY) S += ps[c] * (double)exp2f((mc - M) * kLog2e);
+    DF S{0.f, 0.f};
+    for (int cc = lane; cc < vc; cc += 32) {
+      const float mc = p.pm[row * vc + cc];
+      if (mc > -INFINITY) {
+        const float2 sc = p.ps[row * vc + cc];
+        S = df_add(S, df_mulf(DF{sc.x, sc.y}, exp2f((mc - M) * kLog2e)));
+      }
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) S += __shfl_xor_sync(0xffffffffu, S, off);
+    for (int off = 16; off > 0; off >>= 1)
+      S = df_add(S, DF{__shfl_xor_sync(0xffffffffu, S.hi, off), __shfl_xor_sync(0xffffffffu, S.lo, off)});
+    // S >= 1: the chunk holding M contributes at least exp(0)
     const bool all_ninf = !(M > -INFINITY);
-    const double lse = all_ninf ? -INFINITY : (double)M + log(S);
-    const float* pv = p.pv + row * vc * kXK;
-    const int32_t* pi = p.pi + row * vc * kXK;
-    int p0 = 0, p1 = 0;                            // heads of chunks lane and lane + 32
-    int cnt = 0;
+    const DF lse = all_ninf ? DF{-INFINITY, 0.f} : df_add(DF{M, 0.f}, df_log_ge1(S));
+    __syncwarp();
+    // lane l walks the lists of chunks l and l + 32; lane r keeps the r-th
+    // winner
+    int q0 = 0, q1 = 0;
+    int nvalid = 0;
+    Ent won{-INFINITY, -1};                        // lane r keeps the r-th winner
     for (int r = 0; r < K; ++r) {
       const int c0 = lane, c1 = lane + 32;
-      const Ent h0 = (c0 < vc && p0 < K) ? Ent{pv[(int64_t)c0 * kXK + p0], pi[(int64_t)c0 * kXK + p0]}
-                                         : Ent{-INFINITY, -1};
-      const Ent h1 = (c1 < vc && p1 < K) ? Ent{pv[(int64_t)c1 * kXK + p1], pi[(int64_t)c1 * kXK + p1]}
-                                         : Ent{-INFINITY, -1};
+      const Ent h0 = (c0 < vc && q0 < K) ? Ent{w_v[warp][c0 * K + q0], w_i[warp][c0 * K + q0]} : Ent{-INFINITY, -1};
+      const Ent h1 = (c1 < vc && q1 < K) ? Ent{w_v[warp][c1 * K + q1], w_i[warp][c1 * K + q1]} : Ent{-INFINITY, -1};
       const Ent h = ent_before(h1, h0) ? h1 : h0;
       const Ent best = warp_first(h);
       if (best.i < 0) break;                       // the row has no more valid entries
-      if (h0.i == best.i) ++p0;
-      else if (h1.i == best.i) ++p1;
-      if (lane == 0) {
-        const int sl = j * K + r;
-        c_cum[sl] = all_ninf ? -INFINITY : s_exp_cum[j] + ((double)best.v - lse);
-        c_token[sl] = p.token_map ? p.token_map[best.i] : best.i;
-        c_parent[sl] = s_exp_node[j];
-        c_depth[sl] = s_exp_depth[j] + 1;
-        c_order[sl] = s_gen + sl;
-      }
-      cnt = r + 1;
+      if (h0.i == best.i) ++q0;
+      else if (h1.i == best.i) ++q1;
+      if (lane == r) won = best;
+      nvalid = r + 1;
     }
-    if (lane == 0) s_count[j] = cnt;
+    // the children, one per lane: cumulative log-probability = parent's +
+    // (logit - lse); -inf when the row (or the logit, or the parent) has
+    // probability 0
+    if (lane < nvalid) {
+      const int sl = j * K + lane;
+      DF cv;
+      if (all_ninf || won.v == -INFINITY || s_exp_cum[j].hi == -INFINITY) cv = DF{-INFINITY, 0.f};
+      else cv = df_add(s_exp_cum[j], df_add(DF{won.v, 0.f}, df_neg(lse)));
+      c_cum[sl] = cv;
+      c_key[sl] = df_key(cv);
+      c_token[sl] = p.token_map ? p.token_map[won.i] : won.i;
+      c_parent[sl] = s_exp_node[j];
+      c_depth[sl] = s_exp_depth[j] + 1;
+      c_order[sl] = s_gen + sl;
+    }
+    if (lane == 0) s_count[j] = nvalid;
+    __syncwarp();
   }
   __syncthreads();
 
@@ -418,37 +653,43 @@ __global__ __launch_bounds__(kXThreads) void expand_step_kernel(XParams p) {
   const int keep = p.N - s_n;
   int pops = p.W < keep ? p.W : keep;
   if (pops > total) pops = total;
-  __shared__ double n_cum[kXN];
+  __shared__ DF n_cum[kXN];
   __shared__ int n_parent[kXN], n_token[kXN], n_depth[kXN], n_order[kXN];
   for (int t = tid; t < P + E * K; t += blockDim.x) {
-    double c;
+    DF c;
+    uint64_t kk;
     int o, pa, tk, dp, rank;
     if (t < P) {
       c = q_cum[t];
+      kk = q_key[t];
       o = q_order[t];
       pa = q_parent[t];
       tk = q_token[t];
       dp = q_depth[t];
       rank = t;
-      for (int j = 0; j < E; ++j) rank += count_before(c_cum + j * K, c_order + j * K, s_count[j], c, o);
+      for (int j = 0; j < E; ++j) rank += count_before(c_key + j * K, c_order + j * K, s_count[j], kk, o);
     } else {
       const int sl = t - P, j = sl / K, r = sl - j * K;
       if (r >= s_count[j]) continue;
       c = c_cum[sl];
+      kk = c_key[sl];
       o = c_order[sl];
       pa = c_parent[sl];
       tk = c_token[sl];
       dp = c_depth[sl];
-      rank = r + count_before(q_cum, q_order, P, c, o);
+      rank = r + count_before(q_key, q_order, P, kk, o);
       for (int j2 = 0; j2 < E; ++j2)
-        if (j2 != j) rank += count_before(c_cum + j2 * K, c_order + j2 * K, s_count[j2], c, o);
+        if (j2 != j) rank += count_before(c_key + j2 * K, c_order + j2 * K, s_count[j2], kk, o);
     }
     if (rank < pops) {
       const int i = s_n + rank;
       tok[i] = tk;
       par[i] = pa;
       dep[i] = dp;
-      cum[i] = c;
+      cum[i] = (double)c.hi + (double)c.lo;
+      st->node_hi[i] = c.hi;
+      st->node_lo[i] = c.lo;
+      st->node_depth[i] = dp;
     } else if (rank < keep) {
       const int q = rank - pops;
       n_cum[q] = c;
@@ -461,7 +702,8 @@ __global__ __launch_bounds__(kXThreads) void expand_step_kernel(XParams p) {
   __syncthreads();
   const int remain = (total < keep ? total : keep) - pops;
   if (tid < remain) {
-    st->pool_cum[tid] = n_cum[tid];
+    st->pool_hi[tid] = n_cum[tid].hi;
+    st->pool_lo[tid] = n_cum[tid].lo;
     st->pool_parent[tid] = n_parent[tid];
     st->pool_token[tid] = n_token[tid];
     st->pool_depth[tid] = n_depth[tid];
@@ -471,6 +713,11 @@ __global__ __launch_bounds__(kXThreads) void expand_step_kernel(XParams p) {
   if (tid == 0) {
     const int n = s_n + pops;
     const int done = n >= p.N || pops == 0;
+    if (p.step == 0) {
+      st->node_hi[0] = 0.f;
+      st->node_lo[0] = 0.f;
+      st->node_depth[0] = 0;
+    }
     st->magic = kXMagic;
     st->step = p.step;
     st->n_nodes = n;
@@ -497,15 +744,17 @@ int x_validate(const tv_expand_desc* d) {
   return TV_OK;
 }
 
-// Vocabulary chunks per row: about two CTAs per SM over all rows, at least
-// 1024 entries per chunk, at most kXChunks chunks; chunk lengths are
-// multiples of 8 so 16-byte loads stay aligned.
-void x_chunks(int64_t rows, int V, int* vchunks, int* vlen) {
-  int64_t want = (2 * (int64_t)num_sms() + rows - 1) / rows;
-  int64_t maxc = ((int64_t)V + 1023) / 1024;
-  if (maxc > kXChunks) maxc = kXChunks;
-  if (maxc < 1) maxc = 1;
-  if (want > maxc) want = maxc;
+// Vocabulary chunks per row: one tile (8192 entries) per CTA, so each
+// thread issues all its loads at once and keeps them in registers for both
+// passes; at most min(64, kXRowEntries / K) chunks (the step stages the
+// row's lists in shared memory and each lane walks two of them), larger
+// chunks looping over tiles beyond that.  The row
+// is spread evenly over its chunks (lengths a multiple of 8: 16-byte loads
+// stay aligned), so every warp of a CTA holds entries.
+void x_chunks(int K, int V, int* vchunks, int* vlen) {
+  int64_t want = ((int64_t)V + kXTileElems - 1) / kXTileElems;
+  if (want > kXRowEntries / K) want = kXRowEntries / K;
+  if (want > 64) want = 64;                    // the step's lanes walk two lists each
   if (want < 1) want = 1;
   int64_t len = ((int64_t)V + want - 1) / want;
   len = (len + 7) / 8 * 8;
@@ -521,29 +770,44 @@ XLayout x_layout(const tv_expand_desc* d) {
   const int64_t rows = (int64_t)d->batch * d->width;
   XLayout l;
   int64_t off = 0;
-  l.state = off;
-  off = align_up(off + (int64_t)d->batch * (int64_t)sizeof(XState), 256);
-  l.pv = off;
-  off = align_up(off + rows * kXChunks * kXK * 4, 256);
-  l.pi = off;
-  off = align_up(off + rows * kXChunks * kXK * 4, 256);
-  l.pm = off;
-  off = align_up(off + rows * kXChunks * 4, 256);
-  l.ps = off;
-  off = align_up(off + rows * kXChunks * 8, 256);
+  auto take = [&](int64_t bytes) {
+    const int64_t at = off;
+    off = align_up(off + bytes, 256);
+    return at;
+  };
+  l.state = take((int64_t)d->batch * (int64_t)sizeof(XState));
+  l.pv = take(rows * kXRowEntries * 4);
+  l.pi = take(rows * kXRowEntries * 4);
+  l.pm = take(rows * kXRowEntries * 4);
+  l.ps = take(rows * kXRowEntries * 8);
   l.total = off;
   return l;
 }
 
+struct TopkArgs {
+  const void* logits;
+  int64_t stride;
+  int V, R, vlen, vc, K, vec;
+  float* pv;
+  int32_t* pi;
+  float* pm;
+  float2* ps;
+};
+
+template <bool BF16, int KT>
+cudaError_t launch_topk_kt(dim3 grid, cudaStream_t s, const TopkArgs& a) {
+  return launch_dep(draft_topk_kernel<BF16, KT>, grid, dim3(kXTopkThreads), 0, s, a.logits, a.stride, a.V, a.R,
+                    a.vlen, a.vc, a.K, a.vec, a.pv, a.pi, a.pm, a.ps);
+}
+
 template <bool BF16>
-cudaError_t launch_topk(int KT, dim3 grid, cudaStream_t s, const void* logits, int64_t stride, int V, int R, int vlen,
-                        int vc, int K, int vec, float* pv, int32_t* pi, float* pm, double* ps) {
+cudaError_t launch_topk(int KT, dim3 grid, cudaStream_t s, const TopkArgs& a) {
   switch (KT) {
-    case 1: return launch_dep(draft_topk_kernel<BF16, 1>, grid, dim3(kXThreads), 0, s, logits, stride, V, R, vlen, vc, K, vec, pv, pi, pm, ps);
-    case 2: return launch_dep(draft_topk_kernel<BF16, 2>, grid, dim3(kXThreads), 0, s, logits, stride, V, R, vlen, vc, K, vec, pv, pi, pm, ps);
-    case 4: return launch_dep(draft_topk_kernel<BF16, 4>, grid, dim3(kXThreads), 0, s, logits, stride, V, R, vlen, vc, K, vec, pv, pi, pm, ps);
-    case 8: return launch_dep(draft_topk_kernel<BF16, 8>, grid, dim3(kXThreads), 0, s, logits, stride, V, R, vlen, vc, K, vec, pv, pi, pm, ps);
-    default: return launch_dep(draft_topk_kernel<BF16, 16>, grid, dim3(kXThreads), 0, s, logits, stride, V, R, vlen, vc, K, vec, pv, pi, pm, ps);
+    case 1: return launch_topk_kt<BF16, 1>(grid, s, a);
+    case 2: return launch_topk_kt<BF16, 2>(grid, s, a);
+    case 4: return launch_topk_kt<BF16, 4>(grid, s, a);
+    case 8: return launch_topk_kt<BF16, 8>(grid, s, a);
+    default: return launch_topk_kt<BF16, 16>(grid, s, a);
   }
 }
 
@@ -609,27 +873,34 @@ int tv_tree_expand_step(const tv_expand_desc* desc, int32_t step, const void* d_
   if ((int64_t)workspace_bytes < l.total) return TV_ERR_WORKSPACE;
 
   char* ws = static_cast<char*>(d_workspace);
-  float* pv = reinterpret_cast<float*>(ws + l.pv);
-  int32_t* pi = reinterpret_cast<int32_t*>(ws + l.pi);
-  float* pm = reinterpret_cast<float*>(ws + l.pm);
-  double* ps = reinterpret_cast<double*>(ws + l.ps);
   const int64_t rows = (int64_t)desc->batch * R;
-  int vc = 1, vlen = V;
-  x_chunks(rows, V, &vc, &vlen);
+  TopkArgs ta;
+  ta.logits = d_logits;
+  ta.stride = seq_stride;
+  ta.V = V;
+  ta.R = R;
+  x_chunks(desc->top_k, V, &ta.vc, &ta.vlen);
+  ta.K = desc->top_k;
+  // 16-byte loads when rows stay aligned and every thread gets a vector of
+  // the first tile (else one entry per thread and step, which spreads short
+  // chunks over all warps)
+  ta.vec = ((int64_t)V * ES) % 16 == 0 && (seq_stride * ES) % 16 == 0 && ta.vlen >= kXTopkThreads * (16 / ES);
+  ta.pv = reinterpret_cast<float*>(ws + l.pv);
+  ta.pi = reinterpret_cast<int32_t*>(ws + l.pi);
+  ta.pm = reinterpret_cast<float*>(ws + l.pm);
+  ta.ps = reinterpret_cast<float2*>(ws + l.ps);
   const int K = desc->top_k;
   const int KT = K <= 1 ? 1 : K <= 2 ? 2 : K <= 4 ? 4 : K <= 8 ? 8 : 16;
-  const int vec = ((int64_t)V * ES) % 16 == 0 && (seq_stride * ES) % 16 == 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const dim3 grid(vc, (unsigned)rows);
-  cudaError_t e = desc->logits_dtype == TV_BF16
-                      ? launch_topk<true>(KT, grid, s, d_logits, seq_stride, V, R, vlen, vc, K, vec, pv, pi, pm, ps)
-                      : launch_topk<false>(KT, grid, s, d_logits, seq_stride, V, R, vlen, vc, K, vec, pv, pi, pm, ps);
+  const dim3 grid(ta.vc, (unsigned)rows);
+  cudaError_t e = desc->logits_dtype == TV_BF16 ? launch_topk<true>(KT, grid, s, ta) : launch_topk<false>(KT, grid, s, ta);
   if (e != cudaSuccess) return TV_ERR_CUDA;
   XParams xp;
-  xp.pv = pv;
-  xp.pi = pi;
-  xp.pm = pm;
-  xp.ps = ps;
+  xp.pv = ta.pv;
+  xp.pi = ta.pi;
+  xp.pm = ta.pm;
+  xp.ps = ta.ps;
+  xp.vchunks = ta.vc;
   xp.root_tokens = d_root_tokens;
   xp.token_map = d_token_map;
   xp.tokens = d_tokens;
@@ -642,7 +913,6 @@ int tv_tree_expand_step(const tv_expand_desc* desc, int32_t step, const void* d_
   xp.status = d_status;
   xp.step = step;
   xp.R = R;
-  xp.vchunks = vc;
   xp.K = K;
   xp.W = desc->width;
   xp.N = desc->max_nodes;

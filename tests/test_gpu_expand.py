@@ -3,7 +3,7 @@
 Tokens, parents, depths, node counts and the order nodes enter the tree are
 compared exactly; cumulative log-probabilities within CUM_TOL.  The kernel's
 log-sum-exp differs from the oracle's float64 one by rounding (float32 sums of
-float32 exponentials per thread), so every workload used here is checked
+float32 exponentials within a warp), so every workload used here is checked
 first, by the oracle alone, to make no decision between two candidates whose
 values differ by less than DECIDE (a gap of exactly 0 is a tie between
 siblings with equal logits, which both sides compute from identical numbers
@@ -122,6 +122,19 @@ def test_ties_go_to_smaller_tokens_and_first_generated():
     refs = oracle_trees(spec, rows)
     check(spec, dx, refs)
     assert refs[0]["tokens"][1:4] == [0, 1, 2]
+
+
+@pytest.mark.parametrize("V,dtype", [(5000, "bf16"), (9000, "f32")])
+def test_rows_of_equal_logits(V, dtype):
+    # a whole chunk of equal logits (more candidates than one CTA ranks
+    # directly): the smaller tokens still win, in order
+    spec = wl.ExpandSpec("x-flat", 2, V, 16, 4, 30, 4, dtype, 1.0, 21)
+    rows = [torch.full_like(r, 0.5) for r in all_rows(spec, spec.max_nodes + 1)]
+    rows[1][1, 2, 4100:4108] = 0.75          # a few larger entries in the second chunk
+    dx = run(spec, rows=rows)
+    refs = oracle_trees(spec, rows)
+    check(spec, dx, refs)
+    assert refs[0]["tokens"][1:17] == list(range(16))
 
 
 def test_nan_entries_never_chosen_and_empty_rows():
