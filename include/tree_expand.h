@@ -22,9 +22,11 @@
  *   values in increasing token order (the smaller token wins ties), compared
  *   as the raw logits (never a rounded or clamped copy); NaN is never chosen.
  *   Log-probability of token v: logit[v] - log sum_u exp(logit[u]) over the
- *   non-NaN entries (computed with the maximum subtracted; the sum of
- *   exponentials in float32 within a warp and float64 across warps and
- *   vocabulary chunks; the log and the subtraction in float64).
+ *   non-NaN entries (computed with the maximum subtracted).  Precision: the
+ *   exponentials are summed in float32 per thread and in float pairs (hi +
+ *   lo, about 48 significant bits) above that; the log is M + e*ln2 (exact
+ *   split) + logf(mantissa), within about 1e-7; cumulative values are float
+ *   pairs inside the kernels and float64 in d_cum.
  *
  * The drafter is the caller's: between two steps it computes the draft
  * logits of the nodes the previous step moved into the tree.
