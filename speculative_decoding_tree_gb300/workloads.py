@@ -405,3 +405,47 @@ def root_tokens(spec: ExpandSpec) -> torch.Tensor:
     """[B] int32 root (anchor) tokens, uniform over the vocabulary."""
     g = torch.Generator("cpu").manual_seed(spec.seed * 1000003 - 1)
     return torch.randint(0, spec.vocab, (spec.batch,), generator=g, dtype=torch.int64).to(torch.int32)
+
+
+# ----------------------------------------------------------------------------
+# lm_head + argmax: the target model's final hidden rows and output weights
+# ----------------------------------------------------------------------------
+
+@dataclass(frozen=True)
+class LmHeadSpec:
+    """The lm_head step over a verify workload's tree rows: hidden rows
+    [rows, hidden] and output weights [vocab, hidden], both bf16 (random
+    weights of that shape: no trained model is used)."""
+    name: str
+    rows: int
+    hidden: int
+    vocab: int
+    logit_std: float
+    seed: int
+
+    def replace(self, **kw) -> "LmHeadSpec":
+        return dataclasses.replace(self, **kw)
+
+
+LMHEAD_CONFIGS = {
+    # the 64-node EAGLE-2 tree's rows; a Qwen-family 27B-class model (hidden 5120, vocabulary 151936)
+    "qwen": LmHeadSpec("lmhead-bf16-h5120-v151936-r64", 64, 5120, 151936, 3.0, 3001),
+    # the batched workload's 16 trees (612 rows); a Llama-family 8B-class model (hidden 4096, vocabulary 128256)
+    "batched": LmHeadSpec("lmhead-bf16-h4096-v128256-r612", 612, 4096, 128256, 3.0, 3002),
+}
+
+
+def lm_head_inputs(spec: LmHeadSpec):
+    """(hidden [rows, hidden] bf16, weight [vocab, hidden] bf16): hidden rows
+    N(0, 1); weights N(0, logit_std^2 / hidden) so that logits have standard
+    deviation about logit_std.  Drawn in fp32 from
+    torch.Generator('cpu').manual_seed(seed) (hidden first, then the weights
+    in blocks of 8192 rows) and cast with round-to-nearest-even."""
+    g = torch.Generator("cpu").manual_seed(spec.seed)
+    hidden = torch.randn(spec.rows, spec.hidden, generator=g).to(torch.bfloat16)
+    w = torch.empty(spec.vocab, spec.hidden, dtype=torch.bfloat16)
+    sd = spec.logit_std / math.sqrt(spec.hidden)
+    for v0 in range(0, spec.vocab, 8192):
+        v1 = min(spec.vocab, v0 + 8192)
+        w[v0:v1] = (torch.randn(v1 - v0, spec.hidden, generator=g) * sd).to(torch.bfloat16)
+    return hidden, w
