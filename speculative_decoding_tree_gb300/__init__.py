@@ -1,8 +1,8 @@
 """Tree-verify step of tree speculative decoding on GB300 (sm_103a).
 
 A thin ctypes binding over libtreeverify.so, whose C ABI is declared in
-include/tree_verify.h (the verify step) and include/tree_expand.h (dynamic
-draft-tree expansion).  Every function here only marshals arguments (torch
+include/tree_verify.h (the verify step), include/tree_expand.h (dynamic
+draft-tree expansion) and include/tree_lm_head.h (fused lm_head + argmax).  Every function here only marshals arguments (torch
 tensors or raw device addresses, a stream) and raises on a non-zero status;
 all work happens in the library's CUDA kernels.  There is no CPU fallback:
 calling into a library that was not built raises ``LibraryNotBuilt``.
@@ -17,7 +17,8 @@ __all__ = [
     "lib", "make_desc", "tv_workspace_size", "tv_attn_plan", "tv_status_string", "tv_version",
     "tv_build_tree_mask", "tree_verify_attn", "tv_attn_partials", "tv_attn_merge", "tree_accept_commit",
     "tree_accept_commit_sampled", "TvExpandDesc", "make_expand_desc", "tv_expand_workspace_size",
-    "tv_expand_steps", "tv_tree_expand_step",
+    "tv_expand_steps", "tv_tree_expand_step", "TvLmHeadDesc", "make_lmhead_desc", "tv_lm_head_workspace_size",
+    "tv_lm_head_argmax",
 ]
 
 F32, BF16 = 0, 1
@@ -56,6 +57,10 @@ class TvExpandDesc(ctypes.Structure):
                 ("batch", "vocab", "top_k", "width", "max_nodes", "max_depth", "logits_dtype")]
 
 
+class TvLmHeadDesc(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("rows", "hidden", "vocab")]
+
+
 _LIB = None
 _P = ctypes.c_void_p
 _I = ctypes.c_int32
@@ -73,6 +78,8 @@ _SIG = {
     "tv_expand_steps": [ctypes.POINTER(TvExpandDesc), ctypes.POINTER(ctypes.c_int32)],
     "tv_tree_expand_step": [ctypes.POINTER(TvExpandDesc), _I, _P, ctypes.c_int64] + [_P] * 9
                            + [ctypes.c_size_t, _P, _P],
+    "tv_lm_head_workspace_size": [ctypes.POINTER(TvLmHeadDesc), ctypes.POINTER(ctypes.c_size_t)],
+    "tv_lm_head_argmax": [ctypes.POINTER(TvLmHeadDesc)] + [_P] * 5 + [ctypes.c_size_t, _P, _P],
 }
 
 
@@ -218,3 +225,19 @@ def tv_tree_expand_step(desc, step, logits, seq_stride, root_tokens, token_map, 
                                      _ptr(root_tokens), _ptr(token_map), _ptr(tokens), _ptr(parents), _ptr(depths),
                                      _ptr(cum), _ptr(n_nodes), _ptr(expand_count), _ptr(workspace),
                                      int(workspace_bytes), _ptr(status), _stream(stream)), "tv_tree_expand_step")
+
+
+def make_lmhead_desc(*, rows, hidden, vocab) -> TvLmHeadDesc:
+    return TvLmHeadDesc(rows, hidden, vocab)
+
+
+def tv_lm_head_workspace_size(desc: TvLmHeadDesc) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().tv_lm_head_workspace_size(ctypes.byref(desc), ctypes.byref(n)), "tv_lm_head_workspace_size")
+    return n.value
+
+
+def tv_lm_head_argmax(desc, hidden, weight, argmax, max_logit, workspace, workspace_bytes, status, stream=None):
+    _check(lib().tv_lm_head_argmax(ctypes.byref(desc), _ptr(hidden), _ptr(weight), _ptr(argmax), _ptr(max_logit),
+                                   _ptr(workspace), int(workspace_bytes), _ptr(status), _stream(stream)),
+           "tv_lm_head_argmax")

@@ -12,7 +12,8 @@ import torch
 
 from . import (BF16, F32, make_desc, make_expand_desc, tree_accept_commit, tree_accept_commit_sampled,
                tree_verify_attn, tv_attn_merge, tv_attn_partials, tv_build_tree_mask, tv_expand_steps,
-               tv_expand_workspace_size, tv_tree_expand_step, tv_workspace_size)
+               tv_expand_workspace_size, tv_tree_expand_step, tv_workspace_size, make_lmhead_desc,
+               tv_lm_head_argmax, tv_lm_head_workspace_size)
 
 _DT = {torch.float32: F32, torch.bfloat16: BF16}
 
@@ -142,6 +143,31 @@ class DeviceExpand:
             self.step(s, stream)
 
 
+class DeviceLmHead:
+    """Device buffers of one lm_head workload (workloads.LmHeadSpec): hidden
+    rows and weights resident, the argmax and max-logit outputs, the
+    workspace; run() is one tv_lm_head_argmax call."""
+
+    def __init__(self, spec, device="cuda", hidden=None, weight=None):
+        from . import workloads as wl
+        dev = torch.device(device)
+        self.spec = spec
+        if hidden is None or weight is None:
+            hidden, weight = wl.lm_head_inputs(spec)
+        self.hidden = hidden.to(dev).contiguous()
+        self.weight = weight.to(dev).contiguous()
+        self.desc = make_lmhead_desc(rows=spec.rows, hidden=spec.hidden, vocab=spec.vocab)
+        self.argmax = torch.zeros(spec.rows, dtype=torch.int32, device=dev)
+        self.max_logit = torch.zeros(spec.rows, dtype=torch.float32, device=dev)
+        self.status = torch.zeros(4, dtype=torch.int32, device=dev)
+        self.ws_bytes = tv_lm_head_workspace_size(self.desc)
+        self.workspace = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
+
+    def run(self, stream=None, weight=None):
+        tv_lm_head_argmax(self.desc, self.hidden, self.weight if weight is None else weight, self.argmax,
+                          self.max_logit, self.workspace, self.ws_bytes, self.status, stream)
+
+
 def main(argv=None):
     """Run one seeded input set of a workload through the verify step a few
     times (e.g. under a profiler): python -m speculative_decoding_tree_gb300.runner
@@ -158,8 +184,17 @@ def main(argv=None):
     ap.add_argument("--sampled", type=float, default=0.0,
                     help="temperature > 0: sampled verification (tree_accept_commit_sampled)")
     ap.add_argument("--expand", default="", help="run a dynamic-expansion workload instead (eagle2, batched)")
+    ap.add_argument("--lm-head", default="", help="run a fused lm_head + argmax workload instead (qwen, batched)")
     a = ap.parse_args(argv)
     _build.build()
+    if a.lm_head:
+        lm = DeviceLmHead(wl.LMHEAD_CONFIGS[a.lm_head])
+        for _ in range(a.steps):
+            lm.run()
+        torch.cuda.synchronize()
+        status = int(lm.status[0].item())
+        print(f"{lm.spec.name}: {a.steps} calls, device status {status}")
+        return 0 if status == 0 else 1
     if a.expand:
         dx = DeviceExpand(wl.EXPAND_CONFIGS[a.expand])
         for _ in range(a.steps):
