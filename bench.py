@@ -258,6 +258,67 @@ def expansion_timing(cap_stream, reps=5, trees_per_graph=8):
     return out
 
 
+def bf16_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def lm_head_timing(cap_stream, peak, reps=5, calls=6):
+    """Fused lm_head + argmax: `calls` back-to-back calls in one CUDA graph,
+    CUDA events; per call = total / calls.  The weights (1 to 1.6 GB) are far
+    larger than L2, so every call streams them from HBM.  Algorithmic bytes
+    per call: the weights, the hidden rows and the argmax / max-logit
+    outputs."""
+    from speculative_decoding_tree_gb300.runner import DeviceLmHead
+    out = {}
+    for key in ("qwen", "batched"):
+        spec = wl.LMHEAD_CONFIGS[key]
+        lm = DeviceLmHead(spec)
+        lm.run()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap_stream):
+            for _ in range(calls):
+                lm.run()
+        g.replay()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda._sleep(2_000_000)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3 / calls)
+        us = statistics.median(ts)
+        wbytes = spec.vocab * spec.hidden * 2
+        algo = wbytes + spec.rows * spec.hidden * 2 + spec.rows * 8
+        flops = 2.0 * spec.rows * spec.vocab * spec.hidden
+        gbs = algo / (us * 1e-6) / 1e9
+        tflops = flops / (us * 1e-6) / 1e12
+        tpeak, tkind = bf16_peak()
+        # the bound: weight streaming below the ridge (peak flop/s over peak
+        # bytes/s), the tensor cores above it
+        tensor = flops / algo > tpeak * 1e12 / (peak * 1e9)
+        out[key] = {"workload": spec.name, "rows": spec.rows, "hidden": spec.hidden, "vocab": spec.vocab,
+                    "us": round(us, 2), "algorithmic_bytes": algo, "flops": flops, "gbs": round(gbs, 1),
+                    "tflops": round(tflops, 1),
+                    "roofline": {"bound": "tensor" if tensor else "hbm",
+                                 "achieved": round(tflops if tensor else gbs, 1),
+                                 "peak": tpeak if tensor else peak, "unit": "TFLOP/s" if tensor else "GB/s",
+                                 "frac": round(tflops / tpeak if tensor else gbs / peak, 4),
+                                 "peak_source": tkind if tensor else "measured"},
+                    "launches": 2, "device_status": int(lm.status[0].item())}
+        del lm, g
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, ws, rank):
     import numpy as np  # noqa: F401
     from speculative_decoding_tree_gb300 import _build
@@ -397,6 +458,7 @@ def run_ours(args, ws, rank):
         st_.prefix_len.copy_(st_.p0)
     del pool
     expansion = expansion_timing(cap_stream)
+    lm_heads = lm_head_timing(cap_stream, measured_peaks()[0])
     timing_mode = ("back-to-back launches of each call in one CUDA graph over the rotating input sets, "
                    "programmatic dependent launch between them; per launch = events around the graph / launches")
     clocks = sampler.stop() if sampler else None
@@ -470,8 +532,9 @@ def run_ours(args, ws, rank):
         "accept_commit_us": round(acc_us, 2),
         "accept_commit_sampled_us": round(samp_us, 2),
         "expansion": expansion,
+        "lm_head_argmax": lm_heads,
         "plan": plan,
-        "device_status": status | max(e["device_status"] for e in expansion.values()),
+        "device_status": status | max(e["device_status"] for e in list(expansion.values()) + list(lm_heads.values())),
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(spec, args.cpu_seconds)

@@ -185,10 +185,12 @@ def main(argv=None):
                     help="temperature > 0: sampled verification (tree_accept_commit_sampled)")
     ap.add_argument("--expand", default="", help="run a dynamic-expansion workload instead (eagle2, batched)")
     ap.add_argument("--lm-head", default="", help="run a fused lm_head + argmax workload instead (qwen, batched)")
+    ap.add_argument("--vocab", type=int, default=0, help="with --lm-head: a smaller vocabulary (e.g. for a profiler)")
     a = ap.parse_args(argv)
     _build.build()
     if a.lm_head:
-        lm = DeviceLmHead(wl.LMHEAD_CONFIGS[a.lm_head])
+        spec = wl.LMHEAD_CONFIGS[a.lm_head]
+        lm = DeviceLmHead(spec.replace(vocab=a.vocab, name=f"{spec.name}-v{a.vocab}") if a.vocab else spec)
         for _ in range(a.steps):
             lm.run()
         torch.cuda.synchronize()
