@@ -2,7 +2,8 @@
 
 A thin ctypes binding over libtreeverify.so, whose C ABI is declared in
 include/tree_verify.h (the verify step), include/tree_expand.h (dynamic
-draft-tree expansion) and include/tree_lm_head.h (fused lm_head + argmax).  Every function here only marshals arguments (torch
+draft-tree expansion), include/tree_lm_head.h (fused lm_head + argmax) and
+include/tree_rope.h (tree-position RoPE and the K/V scatter).  Every function here only marshals arguments (torch
 tensors or raw device addresses, a stream) and raises on a non-zero status;
 all work happens in the library's CUDA kernels.  There is no CPU fallback:
 calling into a library that was not built raises ``LibraryNotBuilt``.
@@ -18,7 +19,7 @@ __all__ = [
     "tv_build_tree_mask", "tree_verify_attn", "tv_attn_partials", "tv_attn_merge", "tree_accept_commit",
     "tree_accept_commit_sampled", "TvExpandDesc", "make_expand_desc", "tv_expand_workspace_size",
     "tv_expand_steps", "tv_tree_expand_step", "TvLmHeadDesc", "make_lmhead_desc", "tv_lm_head_workspace_size",
-    "tv_lm_head_argmax",
+    "tv_lm_head_argmax", "tv_tree_rope_scatter",
 ]
 
 F32, BF16 = 0, 1
@@ -80,6 +81,7 @@ _SIG = {
                            + [ctypes.c_size_t, _P, _P],
     "tv_lm_head_workspace_size": [ctypes.POINTER(TvLmHeadDesc), ctypes.POINTER(ctypes.c_size_t)],
     "tv_lm_head_argmax": [ctypes.POINTER(TvLmHeadDesc)] + [_P] * 5 + [ctypes.c_size_t, _P, _P],
+    "tv_tree_rope_scatter": [ctypes.POINTER(TvDesc), ctypes.c_double] + [_P] * 11,
 }
 
 
@@ -241,3 +243,10 @@ def tv_lm_head_argmax(desc, hidden, weight, argmax, max_logit, workspace, worksp
     _check(lib().tv_lm_head_argmax(ctypes.byref(desc), _ptr(hidden), _ptr(weight), _ptr(argmax), _ptr(max_logit),
                                    _ptr(workspace), int(workspace_bytes), _ptr(status), _stream(stream)),
            "tv_lm_head_argmax")
+
+
+def tv_tree_rope_scatter(desc, theta, q_in, k_in, v_in, prefix_len, node_offsets, depth, q_out, k_tree, v_tree,
+                         status, stream=None):
+    _check(lib().tv_tree_rope_scatter(ctypes.byref(desc), float(theta), _ptr(q_in), _ptr(k_in), _ptr(v_in),
+                                      _ptr(prefix_len), _ptr(node_offsets), _ptr(depth), _ptr(q_out), _ptr(k_tree),
+                                      _ptr(v_tree), _ptr(status), _stream(stream)), "tv_tree_rope_scatter")
