@@ -267,6 +267,32 @@ def bf16_peak():
         return 1900.0, "fallback"
 
 
+def rope_timing(sets, cap_stream, b2b_us):
+    """Tree-position RoPE + K/V scatter for the workload's rows: back-to-back
+    calls over the input sets (queries in place); algorithmic bytes = every
+    Q, K and V element read once and written once, plus the row metadata."""
+    import speculative_decoding_tree_gb300 as tv
+    calls = []
+    nbytes = 0
+    for st_ in sets:
+        R, sp = st_.w.total_rows, st_.w.spec
+        k_in = torch.randn(R, sp.hkv, sp.d, device=st_.q.device).to(st_.q.dtype)
+        v_in = torch.randn(R, sp.hkv, sp.d, device=st_.q.device).to(st_.q.dtype)
+        kt = torch.empty_like(st_.k_tree)
+        vt = torch.empty_like(st_.v_tree)
+        st_.mask()
+
+        def call(st_=st_, k_in=k_in, v_in=v_in, kt=kt, vt=vt):
+            tv.tv_tree_rope_scatter(st_.desc, 1e6, st_.q, k_in, v_in, st_.prefix_len, st_.node_offsets, st_.depth,
+                                    st_.q, kt, vt, st_.status)
+        calls.append(call)
+        es = st_.q.element_size()
+        nbytes = 2 * R * (sp.hq + 2 * sp.hkv) * sp.d * es + R * 4 * 2
+    torch.cuda.synchronize()
+    us = b2b_us([calls[i % len(calls)] for i in range(max(24, 8 * len(calls)))])
+    return us, nbytes
+
+
 def lm_head_timing(cap_stream, peak, reps=5, calls=6):
     """Fused lm_head + argmax: `calls` back-to-back calls in one CUDA graph,
     CUDA events; per call = total / calls.  The weights (1 to 1.6 GB) are far
@@ -458,6 +484,7 @@ def run_ours(args, ws, rank):
         st_.prefix_len.copy_(st_.p0)
     del pool
     expansion = expansion_timing(cap_stream)
+    rope_us, rope_bytes = rope_timing(sets, cap_stream, b2b_us)
     lm_heads = lm_head_timing(cap_stream, measured_peaks()[0])
     timing_mode = ("back-to-back launches of each call in one CUDA graph over the rotating input sets, "
                    "programmatic dependent launch between them; per launch = events around the graph / launches")
@@ -531,6 +558,8 @@ def run_ours(args, ws, rank):
                       "algorithmic_bytes": ab["attn"]},
         "accept_commit_us": round(acc_us, 2),
         "accept_commit_sampled_us": round(samp_us, 2),
+        "rope_scatter": {"us": round(rope_us, 2), "algorithmic_bytes": rope_bytes,
+                         "gbs": round(rope_bytes / (rope_us * 1e-6) / 1e9, 1), "launches": 1},
         "expansion": expansion,
         "lm_head_argmax": lm_heads,
         "plan": plan,
