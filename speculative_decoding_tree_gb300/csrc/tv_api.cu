@@ -87,8 +87,12 @@ int make_plan(const tv_desc* d, Plan* p) {
     rows_per_tile = 4 * rpw;
   }
   int row_tiles = (d->max_nodes * G + rows_per_tile - 1) / rows_per_tile;
-  // two or more 128-row tiles per KV head: CTA pairs (cta_group::2) share each K/V tile
-  const bool pairs = tc && row_tiles >= 2;
+  // two or more 128-row tiles per KV head: CTA pairs (cta_group::2) share
+  // each K/V tile -- for one sequence.  In a batch the trees differ in size
+  // and a pair whose tree fills one tile leaves its peer idle; one CTA per
+  // tile is faster there even though the larger trees read their K/V twice
+  // (the batched workload: 137 against 159 us)
+  const bool pairs = tc && row_tiles >= 2 && d->batch == 1;
   const int launched_tiles = pairs ? 2 * ((row_tiles + 1) / 2) : row_tiles;
   int64_t units = (int64_t)d->batch * d->num_kv_heads * launched_tiles;
   int64_t sms = num_sms();
