@@ -91,6 +91,11 @@ def max_over_ranks(x, ws):
     return float(t.item())
 
 
+def aggregate(ws, units_per_rank, steps, elapsed_ms_max):
+    """Whole-job throughput: every rank's units over the slowest rank's time."""
+    return ws * units_per_rank * steps / (elapsed_ms_max / 1e3)
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -525,7 +530,7 @@ def run_ours(args, ws, rank):
     ab = algorithmic_bytes(w)
     peak, peak_kind = measured_peaks()
     ms_per_step = elapsed_ms / args.steps
-    value = ws * rows * args.steps / (elapsed_ms / 1e3)
+    value = aggregate(ws, rows, args.steps, elapsed_ms)
     plan = tv.tv_attn_plan(st.desc)
     achieved = ab["split"] / (split_us * 1e-6) / 1e9
     res = {
