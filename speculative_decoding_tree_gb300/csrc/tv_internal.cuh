@@ -121,12 +121,17 @@ __device__ inline bool seq_rows(const int32_t* offs, int b, int R, int max_nodes
 
 // Programmatic dependent launch.  Every kernel of the library is launched
 // with programmatic stream serialization, so its CTAs may start while the
-// previous kernel of the stream is still running.  Each kernel therefore
-// touches no global memory before dep_wait(), which returns once the previous
-// grid has completed and its writes are visible; every CTA calls it, so a
-// grid never completes before its predecessor and the ordering of the whole
-// stream stays transitive.  dep_launch() lets the next kernel's CTAs be
-// scheduled early (they wait in dep_wait for this grid to finish).
+// previous kernel of the stream is still running.  dep_wait() returns once
+// the previous grid has completed and its writes are visible; every CTA
+// calls it, and calls it before dep_launch(), so a grid never completes
+// before its predecessor, and when a kernel's CTAs start, every kernel
+// before its predecessor has completed.  Before dep_wait() a kernel
+// therefore reads only what its immediate predecessor does not write: the
+// caller's inputs (sequence lengths, parents, logits), state an earlier
+// kernel of its own call sequence left two launches back (read from L2,
+// never from L1), and L2 / TMA prefetches, which only warm caches; it writes
+// nothing global.  dep_launch() lets the next kernel's CTAs be scheduled
+// early (they wait in their own dep_wait for this grid to finish).
 __device__ __forceinline__ void dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
