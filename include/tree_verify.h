@@ -265,6 +265,17 @@ int tree_accept_commit_sampled(const tv_desc* desc, int32_t vocab, int32_t logit
                                int32_t* d_tokens, void* d_workspace, size_t workspace_bytes, int32_t* d_status,
                                void* stream);
 
+/* Steps 2 and 3 of tree_accept_commit with the target argmax given instead
+ * of logits, e.g. from tv_lm_head_argmax (tree_lm_head.h), which never
+ * writes the logits: d_argmax [total_rows] int32 is read (not written) and
+ * every other argument, output and error is as for tree_accept_commit.  No
+ * workspace is used. */
+int tree_accept_commit_argmax(const tv_desc* desc, const int32_t* d_argmax, const int32_t* d_draft_tokens,
+                              const int32_t* d_parents, const int32_t* d_node_offsets, const void* d_k_tree,
+                              const void* d_v_tree, void* d_k_cache, void* d_v_cache, const int32_t* d_page_table,
+                              int32_t* d_prefix_len, int32_t* d_accept_len, int32_t* d_path, int32_t* d_tokens,
+                              int32_t* d_status, void* stream);
+
 /* ------------------------------------- attention without a workspace */
 
 /* Size in bytes of the library's static scratch array (file-scope device

@@ -19,7 +19,7 @@ __all__ = [
     "tv_build_tree_mask", "tree_verify_attn", "tv_attn_partials", "tv_attn_merge", "tree_accept_commit",
     "tree_accept_commit_sampled", "TvExpandDesc", "make_expand_desc", "tv_expand_workspace_size",
     "tv_expand_steps", "tv_tree_expand_step", "TvLmHeadDesc", "make_lmhead_desc", "tv_lm_head_workspace_size",
-    "tv_lm_head_argmax", "tv_tree_rope_scatter",
+    "tv_lm_head_argmax", "tv_tree_rope_scatter", "tree_accept_commit_argmax",
 ]
 
 F32, BF16 = 0, 1
@@ -82,6 +82,7 @@ _SIG = {
     "tv_lm_head_workspace_size": [ctypes.POINTER(TvLmHeadDesc), ctypes.POINTER(ctypes.c_size_t)],
     "tv_lm_head_argmax": [ctypes.POINTER(TvLmHeadDesc)] + [_P] * 5 + [ctypes.c_size_t, _P, _P],
     "tv_tree_rope_scatter": [ctypes.POINTER(TvDesc), ctypes.c_double] + [_P] * 11,
+    "tree_accept_commit_argmax": [ctypes.POINTER(TvDesc)] + [_P] * 15,
 }
 
 
@@ -250,3 +251,12 @@ def tv_tree_rope_scatter(desc, theta, q_in, k_in, v_in, prefix_len, node_offsets
     _check(lib().tv_tree_rope_scatter(ctypes.byref(desc), float(theta), _ptr(q_in), _ptr(k_in), _ptr(v_in),
                                       _ptr(prefix_len), _ptr(node_offsets), _ptr(depth), _ptr(q_out), _ptr(k_tree),
                                       _ptr(v_tree), _ptr(status), _stream(stream)), "tv_tree_rope_scatter")
+
+
+def tree_accept_commit_argmax(desc, argmax, draft_tokens, parents, node_offsets, k_tree, v_tree, k_cache, v_cache,
+                              page_table, prefix_len, accept_len, path, tokens, status, stream=None):
+    _check(lib().tree_accept_commit_argmax(ctypes.byref(desc), _ptr(argmax), _ptr(draft_tokens), _ptr(parents),
+                                           _ptr(node_offsets), _ptr(k_tree), _ptr(v_tree), _ptr(k_cache),
+                                           _ptr(v_cache), _ptr(page_table), _ptr(prefix_len), _ptr(accept_len),
+                                           _ptr(path), _ptr(tokens), _ptr(status), _stream(stream)),
+           "tree_accept_commit_argmax")

@@ -432,9 +432,13 @@ __global__ __launch_bounds__(256) void walk_commit_kernel(AcceptParams p) {
     if (tid == 0) p.accept_len[b] = -1;
     return;
   }
-  // argmax of node tid / 4 from chunks c = tid % 4, + 4, ...; max value,
-  // smallest index (better() is order-free), NaN never enters
-  {
+  if (p.given_argmax) {
+    // the caller's argmax (e.g. the fused lm_head's): written by the
+    // previous kernel, so read after the dependency wait
+    if (tid < n) s_am[tid] = p.argmax[o0 + tid];
+  } else {
+    // argmax of node tid / 4 from chunks c = tid % 4, + 4, ...; max value,
+    // smallest index (better() is order-free), NaN never enters
     const int vc = p.vchunks;
     const int i = tid >> 2;
     Best bst{-FLT_MAX, -1};
@@ -589,6 +593,7 @@ cudaError_t launch_tree_mask(const int32_t* parents, const int32_t* offs, uint64
 }
 
 cudaError_t launch_accept_commit(const AcceptParams& p, cudaStream_t s) {
+  if (p.given_argmax) return launch_dep(walk_commit_kernel, dim3(p.B), dim3(256), 0, s, p);
   dim3 grid(p.vchunks, p.R);
   cudaError_t e;
   if (p.sampled)

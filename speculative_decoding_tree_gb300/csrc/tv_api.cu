@@ -279,6 +279,7 @@ int accept_commit_impl(const tv_desc* desc, int32_t vocab, int32_t logits_dtype,
   int64_t off = p.o_part_bytes + p.ml_part_bytes;
   if ((int64_t)workspace_bytes < off + accept_bytes(desc, vocab)) return TV_ERR_WORKSPACE;
   AcceptParams a;
+  a.given_argmax = 0;
   a.sampled = sampled;
   a.inv_temp = sampled ? 1.f / temperature : 0.f;
   a.seed_lo = (uint32_t)seed;
@@ -459,6 +460,36 @@ int tree_accept_commit_sampled(const tv_desc* desc, int32_t vocab, int32_t logit
                             d_parents, d_node_offsets, d_k_tree, d_v_tree, d_k_cache, d_v_cache, d_page_table,
                             d_prefix_len, d_sampled, d_accept_len, d_path, d_tokens, d_workspace, workspace_bytes,
                             d_status, stream);
+}
+
+int tree_accept_commit_argmax(const tv_desc* desc, const int32_t* d_argmax, const int32_t* d_draft_tokens,
+                              const int32_t* d_parents, const int32_t* d_node_offsets, const void* d_k_tree,
+                              const void* d_v_tree, void* d_k_cache, void* d_v_cache, const int32_t* d_page_table,
+                              int32_t* d_prefix_len, int32_t* d_accept_len, int32_t* d_path, int32_t* d_tokens,
+                              int32_t* d_status, void* stream) {
+  int rc = validate(desc);
+  if (rc) return rc;
+  if (!d_argmax || !d_draft_tokens || !d_parents || !d_node_offsets || !d_k_tree || !d_v_tree || !d_k_cache ||
+      !d_v_cache || !d_prefix_len || !d_accept_len || !d_path || !d_tokens || !d_status)
+    return TV_ERR_NULL;
+  if (desc->page_size == kPageSize && !d_page_table) return TV_ERR_NULL;
+  const void* all[] = {d_argmax, d_draft_tokens, d_parents, d_node_offsets, d_k_tree, d_v_tree, d_k_cache,
+                       d_v_cache, d_prefix_len, d_accept_len, d_path, d_tokens, d_status};
+  for (const void* ptr : all)
+    if (!aligned16(ptr)) return TV_ERR_ALIGN;
+  if (d_page_table && !aligned16(d_page_table)) return TV_ERR_ALIGN;
+  AcceptParams a = {};
+  a.given_argmax = 1;
+  a.draft = d_draft_tokens; a.parents = d_parents; a.node_offsets = d_node_offsets;
+  a.k_tree = d_k_tree; a.v_tree = d_v_tree; a.k_cache = d_k_cache; a.v_cache = d_v_cache;
+  a.page_table = desc->page_size ? d_page_table : nullptr;
+  a.prefix_len = d_prefix_len; a.argmax = const_cast<int32_t*>(d_argmax); a.accept_len = d_accept_len;
+  a.path = d_path; a.tokens = d_tokens; a.status = d_status;
+  a.B = desc->batch; a.R = desc->total_rows; a.Hkv = desc->num_kv_heads; a.d = desc->head_dim;
+  a.esize = desc->dtype == TV_BF16 ? 2 : 4; a.max_nodes = desc->max_nodes; a.paged = desc->page_size != 0;
+  a.capacity = desc->capacity; a.num_pages = desc->num_pages; a.max_pages = desc->capacity / kPageSize;
+  cudaError_t e = launch_accept_commit(a, as_stream(stream));
+  return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -196,6 +196,7 @@ struct AcceptParams {
   int sampled;               // draw per row (Gumbel-max) instead of the argmax
   float inv_temp;            // 1 / temperature (sampled)
   uint32_t seed_lo, seed_hi, off_lo, off_hi;   // Philox key and counter words 2, 3 (sampled)
+  int given_argmax;          // argmax is an input (no logits pass): only the walk and commit run
 };
 
 cudaError_t launch_accept_commit(const AcceptParams& p, cudaStream_t s);

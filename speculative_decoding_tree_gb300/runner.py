@@ -13,7 +13,7 @@ import torch
 from . import (BF16, F32, make_desc, make_expand_desc, tree_accept_commit, tree_accept_commit_sampled,
                tree_verify_attn, tv_attn_merge, tv_attn_partials, tv_build_tree_mask, tv_expand_steps,
                tv_expand_workspace_size, tv_tree_expand_step, tv_workspace_size, make_lmhead_desc,
-               tv_lm_head_argmax, tv_lm_head_workspace_size)
+               tv_lm_head_argmax, tv_lm_head_workspace_size, tree_accept_commit_argmax)
 
 _DT = {torch.float32: F32, torch.bfloat16: BF16}
 
@@ -88,6 +88,12 @@ class DeviceStep:
                                    self.k_cache, self.v_cache, self.page_table, self.prefix_len, self.argmax,
                                    self.accept_len, self.path, self.tokens, self.workspace, self.ws_bytes,
                                    self.status, stream)
+
+    def accept_commit_argmax(self, argmax, stream=None):
+        """The walk and commit on a given argmax [rows] int32 (device)."""
+        tree_accept_commit_argmax(self.desc, argmax, self.draft, self.parents, self.node_offsets, self.k_tree,
+                                  self.v_tree, self.k_cache, self.v_cache, self.page_table, self.prefix_len,
+                                  self.accept_len, self.path, self.tokens, self.status, stream)
 
     def step(self, stream=None):
         """One verify step: mask, attention, accept + commit."""

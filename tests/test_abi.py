@@ -162,3 +162,16 @@ def test_expand_host_checks(L):
     assert tv.tv_expand_steps(_xdesc(width=1)) == 63
     assert tv.tv_expand_steps(_xdesc(top_k=1, width=4)) == 63          # a chain: one node per step
     assert tv.tv_expand_steps(_xdesc(max_nodes=1)) == 1
+
+
+def test_accept_commit_argmax_host_checks(L):
+    d = _desc()
+    fake = 1 << 20
+    args = [fake] * 13                             # argmax .. tokens; then status, stream
+    assert L.tree_accept_commit_argmax(None, *args, fake, None) == -1
+    bad = list(args)
+    bad[0] = None                                  # no argmax
+    assert L.tree_accept_commit_argmax(ctypes.byref(d), *bad, fake, None) == -1
+    bad[0] = fake + 4
+    assert L.tree_accept_commit_argmax(ctypes.byref(d), *bad, fake, None) == -11
+    assert L.tree_accept_commit_argmax(ctypes.byref(_desc(dtype=7)), *args, fake, None) == -2
