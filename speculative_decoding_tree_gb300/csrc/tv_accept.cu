@@ -12,6 +12,7 @@
 #include <climits>
 
 #include "tv_internal.cuh"
+#include "tv_accept.cuh"
 
 namespace tv {
 namespace {

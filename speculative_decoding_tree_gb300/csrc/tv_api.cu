@@ -7,6 +7,7 @@
 
 #include "tree_expand.h"
 #include "tv_internal.cuh"
+#include "tv_accept.cuh"
 
 namespace tv {
 namespace {
