@@ -157,6 +157,15 @@ const char* tv_status_string(int code);
 /* Library version string, e.g. "treeverify 0.1 sm_103a". */
 const char* tv_version(void);
 
+/* Failure detection check: launches one CTA whose thread waits, with the
+ * bounded wait every tensor-core kernel of the library uses, on a shared
+ * memory barrier that nothing completes.  After limit_ns (1 ms .. 10 s) of
+ * GPU time the wait gives up, the kernel ORs TV_DEV_TIMEOUT into *d_status
+ * and ends; the context stays usable.  Returns TV_ERR_SHAPE for a limit out
+ * of range, TV_ERR_NULL / TV_ERR_ALIGN for d_status, TV_ERR_CUDA if the
+ * launch fails, else TV_OK. */
+int tv_check_bounded_wait(int64_t limit_ns, int32_t* d_status, void* stream);
+
 /* ------------------------------------------------------- A0: tree mask */
 
 /* For every node i of every sequence: d_anc[row] has bit j set iff j == i or

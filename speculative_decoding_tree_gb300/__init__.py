@@ -19,7 +19,7 @@ __all__ = [
     "tv_build_tree_mask", "tree_verify_attn", "tv_attn_partials", "tv_attn_merge", "tree_accept_commit",
     "tree_accept_commit_sampled", "TvExpandDesc", "make_expand_desc", "tv_expand_workspace_size",
     "tv_expand_steps", "tv_tree_expand_step", "TvLmHeadDesc", "make_lmhead_desc", "tv_lm_head_workspace_size",
-    "tv_lm_head_argmax", "tv_tree_rope_scatter", "tree_accept_commit_argmax",
+    "tv_lm_head_argmax", "tv_tree_rope_scatter", "tree_accept_commit_argmax", "tv_check_bounded_wait",
 ]
 
 F32, BF16 = 0, 1
@@ -83,6 +83,7 @@ _SIG = {
     "tv_lm_head_argmax": [ctypes.POINTER(TvLmHeadDesc)] + [_P] * 5 + [ctypes.c_size_t, _P, _P],
     "tv_tree_rope_scatter": [ctypes.POINTER(TvDesc), ctypes.c_double] + [_P] * 11,
     "tree_accept_commit_argmax": [ctypes.POINTER(TvDesc)] + [_P] * 15,
+    "tv_check_bounded_wait": [ctypes.c_int64, _P, _P],
 }
 
 
@@ -260,3 +261,7 @@ def tree_accept_commit_argmax(desc, argmax, draft_tokens, parents, node_offsets,
                                            _ptr(v_cache), _ptr(page_table), _ptr(prefix_len), _ptr(accept_len),
                                            _ptr(path), _ptr(tokens), _ptr(status), _stream(stream)),
            "tree_accept_commit_argmax")
+
+
+def tv_check_bounded_wait(limit_ns, status, stream=None):
+    _check(lib().tv_check_bounded_wait(int(limit_ns), _ptr(status), _stream(stream)), "tv_check_bounded_wait")

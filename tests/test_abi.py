@@ -175,3 +175,11 @@ def test_accept_commit_argmax_host_checks(L):
     bad[0] = fake + 4
     assert L.tree_accept_commit_argmax(ctypes.byref(d), *bad, fake, None) == -11
     assert L.tree_accept_commit_argmax(ctypes.byref(_desc(dtype=7)), *args, fake, None) == -2
+
+
+def test_bounded_wait_check_host_checks(L):
+    fake = 1 << 20
+    assert L.tv_check_bounded_wait(999_999, fake, None) == -6
+    assert L.tv_check_bounded_wait(10_000_000_001, fake, None) == -6
+    assert L.tv_check_bounded_wait(20_000_000, None, None) == -1
+    assert L.tv_check_bounded_wait(20_000_000, fake + 4, None) == -11

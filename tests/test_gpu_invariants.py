@@ -168,3 +168,18 @@ def test_growing_scores_force_rescale(d, nodes, kernel):
     st = run(w)
     assert tv.tv_attn_plan(st.desc)["kernel"] == kernel
     check_step(w, st, oracle.verify_step(w))
+
+
+def test_bounded_wait_runs_out_and_the_context_stays_usable():
+    # failure detection without a fault: a wait that nothing completes ends
+    # after its limit with TV_DEV_TIMEOUT, and the next calls run normally
+    import time
+    import speculative_decoding_tree_gb300 as tv
+    st = torch.zeros(4, dtype=torch.int32, device="cuda")
+    t0 = time.perf_counter()
+    tv.tv_check_bounded_wait(20_000_000, st)
+    torch.cuda.synchronize()
+    assert time.perf_counter() - t0 >= 0.019
+    assert int(st[0]) == 32
+    w = workload(wl.small_variant(3))
+    check_step(w, run(w), oracle.verify_step(w))
