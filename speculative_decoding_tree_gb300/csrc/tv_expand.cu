@@ -138,24 +138,30 @@ __device__ __forceinline__ float load_logit(const void* base, int64_t e) {
 }
 
 // The top-K pass: CTAs of kXTopkThreads threads, each reading one chunk of
-// one row in tiles of kXTopkThreads * kXTile entries (thread t holds kXTile
-// entries of a tile, in increasing index order).
+// one row in tiles of kXTopkThreads * PT entries (thread t holds PT entries of
+// a tile, in increasing index order; PT = 16, or 32 when a step has so many
+// rows that 16 would take more than two waves of CTAs).
 constexpr int kXTopkThreads = 512;
-constexpr int kXTile = 16;
-constexpr int kXTileElems = kXTopkThreads * kXTile;  // 8192
 constexpr int kXRowEntries = 512;                    // chunks x K per row (the step stages them in shared memory)
 constexpr int kXCand = 1024;                         // candidates a CTA ranks directly
 
-// Loads the thread's entries of one tile (NaN where the chunk ends), with
-// their indices.  vec: 16-byte loads (rows 16-byte aligned).
+// Vocabulary index of entry k of the thread's share of the tile at t0.
 template <bool BF16>
-__device__ __forceinline__ void load_tile(const void* logits, int64_t rbase, int t0, int v1, int vec, float x[kXTile],
-                                          int ix[kXTile]) {
+__device__ __forceinline__ int tile_index(int t0, int k, int vec) {
+  constexpr int VE = 16 / (BF16 ? 2 : 4);
+  if (vec) return t0 + ((k / VE) * kXTopkThreads + (int)threadIdx.x) * VE + (k % VE);
+  return t0 + k * kXTopkThreads + (int)threadIdx.x;
+}
+
+// Loads the thread's PT entries of one tile (NaN where the chunk ends).
+// vec: 16-byte loads (rows 16-byte aligned).
+template <bool BF16, int PT>
+__device__ __forceinline__ void load_tile(const void* logits, int64_t rbase, int t0, int v1, int vec, float x[PT]) {
   constexpr int ES = BF16 ? 2 : 4;
   constexpr int VE = 16 / ES;
   if (vec) {
 #pragma unroll
-    for (int g = 0; g < kXTile / VE; ++g) {
+    for (int g = 0; g < PT / VE; ++g) {
       const int e = t0 + (g * kXTopkThreads + (int)threadIdx.x) * VE;
       if (e + VE <= v1) {
         const uint4 u = *reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(logits) + (rbase + e) * ES);
@@ -175,15 +181,12 @@ __device__ __forceinline__ void load_tile(const void* logits, int64_t rbase, int
 #pragma unroll
         for (int q = 0; q < VE; ++q) x[g * VE + q] = e + q < v1 ? load_logit<BF16>(logits, rbase + e + q) : __int_as_float(0x7fffffff);
       }
-#pragma unroll
-      for (int q = 0; q < VE; ++q) ix[g * VE + q] = e + q;
     }
   } else {
 #pragma unroll
-    for (int g = 0; g < kXTile; ++g) {
+    for (int g = 0; g < PT; ++g) {
       const int e = t0 + g * kXTopkThreads + (int)threadIdx.x;
       x[g] = e < v1 ? load_logit<BF16>(logits, rbase + e) : __int_as_float(0x7fffffff);
-      ix[g] = e;
     }
   }
 }
@@ -201,7 +204,7 @@ __device__ __forceinline__ void load_tile(const void* logits, int64_t rbase, int
 // ((row * vchunks + chunk) * K, -1 indices after the valid entries), the
 // maximum in pm (+inf when the chunk holds +inf) and the sum of
 // exponentials in ps (a double-float: float32 per thread, pairs above).
-template <bool BF16, int KT>
+template <bool BF16, int KT, int PT>
 __global__ __launch_bounds__(kXTopkThreads) void draft_topk_kernel(const void* __restrict__ logits, int64_t seq_stride,
                                                                    int V, int R, int vlen, int vchunks, int K, int vec,
                                                                    float* __restrict__ pv, int32_t* __restrict__ pi,
@@ -233,16 +236,16 @@ __global__ __launch_bounds__(kXTopkThreads) void draft_topk_kernel(const void* _
 
   // pass 1: the thread's first maximum (NaN and +inf excluded); the first
   // tile stays in registers for pass 2
-  float x[kXTile];
-  int ix[kXTile];
+  constexpr int kTileElems = kXTopkThreads * PT;
+  float x[PT];
   float tmax = -INFINITY;
   int tidx = -1;
   bool bad = false;
-  const bool one_tile = v1 - v0 <= kXTileElems;
-  for (int t0 = v0; t0 < v1; t0 += kXTileElems) {
-    load_tile<BF16>(logits, rbase, t0, v1, vec, x, ix);
+  const bool one_tile = v1 - v0 <= kTileElems;
+  for (int t0 = v0; t0 < v1; t0 += kTileElems) {
+    load_tile<BF16, PT>(logits, rbase, t0, v1, vec, x);
 #pragma unroll
-    for (int k = 0; k < kXTile; ++k) {
+    for (int k = 0; k < PT; ++k) {
       const float xv = x[k];
       if (xv != xv) continue;
       if (xv == INFINITY) {
@@ -251,7 +254,7 @@ __global__ __launch_bounds__(kXTopkThreads) void draft_topk_kernel(const void* _
       }
       if (tidx < 0 || xv > tmax) {
         tmax = xv;
-        tidx = ix[k];
+        tidx = tile_index<BF16>(t0, k, vec);
       }
     }
   }
@@ -273,16 +276,16 @@ __global__ __launch_bounds__(kXTopkThreads) void draft_topk_kernel(const void* _
 
   // pass 2: sum of exponentials and candidates
   float s = 0.f;
-  auto scan = [&](void) {
+  auto scan = [&](int t0) {
 #pragma unroll
-    for (int k = 0; k < kXTile; ++k) {
+    for (int k = 0; k < PT; ++k) {
       const float xv = x[k];
       if (!(xv < INFINITY)) continue;            // NaN, +inf
       if (xv > -INFINITY) s += exp2f((xv - M) * kLog2e);
     }
     // candidates (>= T), appended with one shared atomic per warp and entry slot
 #pragma unroll
-    for (int k = 0; k < kXTile; ++k) {
+    for (int k = 0; k < PT; ++k) {
       const float xv = x[k];
       const bool cand = xv < INFINITY && xv >= T;  // not NaN, not +inf
       const uint32_t m = __ballot_sync(0xffffffffu, cand);
@@ -294,17 +297,17 @@ __global__ __launch_bounds__(kXTopkThreads) void draft_topk_kernel(const void* _
         const int pos = base + __popc(m & ((1u << lane) - 1u));
         if (pos < kXCand) {
           cv[pos] = xv;
-          ci[pos] = ix[k];
+          ci[pos] = tile_index<BF16>(t0, k, vec);
         }
       }
     }
   };
   if (one_tile) {
-    scan();                                      // the tile pass 1 left in registers
+    scan(v0);                                    // the tile pass 1 left in registers
   } else {
-    for (int t0 = v0; t0 < v1; t0 += kXTileElems) {
-      load_tile<BF16>(logits, rbase, t0, v1, vec, x, ix);
-      scan();
+    for (int t0 = v0; t0 < v1; t0 += kTileElems) {
+      load_tile<BF16, PT>(logits, rbase, t0, v1, vec, x);
+      scan(t0);
     }
   }
   DF sw{s, 0.f};
@@ -352,11 +355,11 @@ __global__ __launch_bounds__(kXTopkThreads) void draft_topk_kernel(const void* _
     // many equal entries: per-thread sorted lists, then K rounds of merges
     TopList<KT> L;
     L.init();
-    for (int t0 = v0; t0 < v1; t0 += kXTileElems) {
-      load_tile<BF16>(logits, rbase, t0, v1, vec, x, ix);
+    for (int t0 = v0; t0 < v1; t0 += kTileElems) {
+      load_tile<BF16, PT>(logits, rbase, t0, v1, vec, x);
 #pragma unroll
-      for (int k = 0; k < kXTile; ++k)
-        if (x[k] < INFINITY) L.push(x[k], ix[k]);
+      for (int k = 0; k < PT; ++k)
+        if (x[k] < INFINITY) L.push(x[k], tile_index<BF16>(t0, k, vec));
     }
     for (int r = 0; r < K; ++r) {
       const Ent best = warp_first(L.e[0]);
@@ -716,8 +719,8 @@ int x_validate(const tv_expand_desc* d) {
 // chunks looping over tiles beyond that.  The row
 // is spread evenly over its chunks (lengths a multiple of 8: 16-byte loads
 // stay aligned), so every warp of a CTA holds entries.
-void x_chunks(int K, int V, int* vchunks, int* vlen) {
-  int64_t want = ((int64_t)V + kXTileElems - 1) / kXTileElems;
+void x_chunks(int K, int V, int tile_elems, int* vchunks, int* vlen) {
+  int64_t want = ((int64_t)V + tile_elems - 1) / tile_elems;
   if (want > kXRowEntries / K) want = kXRowEntries / K;
   if (want > 64) want = 64;                    // the step's lanes walk two lists each
   if (want < 1) want = 1;
@@ -759,21 +762,26 @@ struct TopkArgs {
   float2* ps;
 };
 
-template <bool BF16, int KT>
+template <bool BF16, int KT, int PT>
 cudaError_t launch_topk_kt(dim3 grid, cudaStream_t s, const TopkArgs& a) {
-  return launch_dep(draft_topk_kernel<BF16, KT>, grid, dim3(kXTopkThreads), 0, s, a.logits, a.stride, a.V, a.R,
+  return launch_dep(draft_topk_kernel<BF16, KT, PT>, grid, dim3(kXTopkThreads), 0, s, a.logits, a.stride, a.V, a.R,
                     a.vlen, a.vc, a.K, a.vec, a.pv, a.pi, a.pm, a.ps);
 }
 
-template <bool BF16>
-cudaError_t launch_topk(int KT, dim3 grid, cudaStream_t s, const TopkArgs& a) {
+template <bool BF16, int PT>
+cudaError_t launch_topk_pt(int KT, dim3 grid, cudaStream_t s, const TopkArgs& a) {
   switch (KT) {
-    case 1: return launch_topk_kt<BF16, 1>(grid, s, a);
-    case 2: return launch_topk_kt<BF16, 2>(grid, s, a);
-    case 4: return launch_topk_kt<BF16, 4>(grid, s, a);
-    case 8: return launch_topk_kt<BF16, 8>(grid, s, a);
-    default: return launch_topk_kt<BF16, 16>(grid, s, a);
+    case 1: return launch_topk_kt<BF16, 1, PT>(grid, s, a);
+    case 2: return launch_topk_kt<BF16, 2, PT>(grid, s, a);
+    case 4: return launch_topk_kt<BF16, 4, PT>(grid, s, a);
+    case 8: return launch_topk_kt<BF16, 8, PT>(grid, s, a);
+    default: return launch_topk_kt<BF16, 16, PT>(grid, s, a);
   }
+}
+
+template <bool BF16>
+cudaError_t launch_topk(int KT, int PT, dim3 grid, cudaStream_t s, const TopkArgs& a) {
+  return PT == 32 ? launch_topk_pt<BF16, 32>(KT, grid, s, a) : launch_topk_pt<BF16, 16>(KT, grid, s, a);
 }
 
 }  // namespace
@@ -839,12 +847,19 @@ int tv_tree_expand_step(const tv_expand_desc* desc, int32_t step, const void* d_
 
   char* ws = static_cast<char*>(d_workspace);
   const int64_t rows = (int64_t)desc->batch * R;
-  TopkArgs ta;
+  TopkArgs ta = {};
   ta.logits = d_logits;
   ta.stride = seq_stride;
   ta.V = V;
   ta.R = R;
-  x_chunks(desc->top_k, V, &ta.vc, &ta.vlen);
+  // 16 entries per thread, or 32 when 16 would take more than two waves of
+  // CTAs (two resident per SM)
+  int PT = 16;
+  x_chunks(desc->top_k, V, kXTopkThreads * 16, &ta.vc, &ta.vlen);
+  if (rows * ta.vc > 4 * (int64_t)num_sms()) {
+    PT = 32;
+    x_chunks(desc->top_k, V, kXTopkThreads * 32, &ta.vc, &ta.vlen);
+  }
   ta.K = desc->top_k;
   // 16-byte loads when rows stay aligned and every thread gets a vector of
   // the first tile (else one entry per thread and step, which spreads short
@@ -858,7 +873,8 @@ int tv_tree_expand_step(const tv_expand_desc* desc, int32_t step, const void* d_
   const int KT = K <= 1 ? 1 : K <= 2 ? 2 : K <= 4 ? 4 : K <= 8 ? 8 : 16;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const dim3 grid(ta.vc, (unsigned)rows);
-  cudaError_t e = desc->logits_dtype == TV_BF16 ? launch_topk<true>(KT, grid, s, ta) : launch_topk<false>(KT, grid, s, ta);
+  cudaError_t e = desc->logits_dtype == TV_BF16 ? launch_topk<true>(KT, PT, grid, s, ta)
+                                                : launch_topk<false>(KT, PT, grid, s, ta);
   if (e != cudaSuccess) return TV_ERR_CUDA;
   XParams xp;
   xp.pv = ta.pv;
