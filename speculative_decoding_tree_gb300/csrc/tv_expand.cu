@@ -15,8 +15,8 @@
 // The pool never holds more than N - size entries: an entry ranked below
 // that many others can never enter the tree, since every later candidate is
 // inserted, never removed, ahead of it.  So one tree's whole state is a few
-// hundred bytes and a step is one pass of ranks (binary searches in sorted
-// runs) instead of a heap.
+// hundred bytes and a step is one pass of ranks (each entry counts the
+// entries of the union that precede it) instead of a heap.
 #include <cmath>
 #include <cstdint>
 
@@ -416,16 +416,8 @@ __device__ __forceinline__ bool cand_before(uint64_t ka, int oa, uint64_t kb, in
   return ka > kb || (ka == kb && oa < ob);
 }
 
-// Entries of the sorted run (key[0..n), order[0..n)) that precede (k, o).
-__device__ __forceinline__ int count_before(const uint64_t* key, const int* order, int n, uint64_t k, int o) {
-  int lo = 0, hi = n;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (cand_before(key[mid], order[mid], k, o)) lo = mid + 1;
-    else hi = mid;
-  }
-  return lo;
-}
+// Order of an empty candidate slot: such a slot (key 0) precedes nothing.
+constexpr int kXNoOrder = 0x7fffffff;
 
 // grid (B): one CTA per tree.
 __global__ __launch_bounds__(kXThreads) void expand_step_kernel(XParams p) {
@@ -441,11 +433,13 @@ __global__ __launch_bounds__(kXThreads) void expand_step_kernel(XParams p) {
   __shared__ int s_exp_node[kXW], s_exp_depth[kXW], s_count[kXW];
   __shared__ DF s_exp_cum[kXW];
   __shared__ DF c_cum[kXW * kXK];                // new candidates, row j at [j * K, j * K + count_j)
-  __shared__ uint64_t c_key[kXW * kXK];
-  __shared__ int c_parent[kXW * kXK], c_token[kXW * kXK], c_depth[kXW * kXK], c_order[kXW * kXK];
+  __shared__ int c_parent[kXW * kXK], c_token[kXW * kXK], c_depth[kXW * kXK];
   __shared__ DF q_cum[kXN];                      // pending pool (sorted)
-  __shared__ uint64_t q_key[kXN];
-  __shared__ int q_parent[kXN], q_token[kXN], q_depth[kXN], q_order[kXN];
+  __shared__ int q_parent[kXN], q_token[kXN], q_depth[kXN];
+  // keys and orders of the union: pool entry t at slot t, new candidate
+  // sl at slot P + sl (empty slots hold key 0, order kXNoOrder)
+  __shared__ uint64_t u_key[kXN + kXW * kXK];
+  __shared__ int u_ord[kXN + kXW * kXK];
   __shared__ __align__(16) XState s_st;
 
   // The state step - 1 left.  That grid completed before the top-K grid of
@@ -508,11 +502,15 @@ __global__ __launch_bounds__(kXThreads) void expand_step_kernel(XParams p) {
   }
   if (tid < P) {
     q_cum[tid] = DF{s_st.pool_hi[tid], s_st.pool_lo[tid]};
-    q_key[tid] = df_key(q_cum[tid]);
+    u_key[tid] = df_key(q_cum[tid]);
+    u_ord[tid] = s_st.pool_order[tid];
     q_parent[tid] = s_st.pool_parent[tid];
     q_token[tid] = s_st.pool_token[tid];
     q_depth[tid] = s_st.pool_depth[tid];
-    q_order[tid] = s_st.pool_order[tid];
+  }
+  for (int sl = tid; sl < E * K; sl += blockDim.x) {
+    u_key[P + sl] = 0;
+    u_ord[P + sl] = kXNoOrder;
   }
   dep_wait();
   dep_launch();
@@ -603,11 +601,11 @@ __global__ __launch_bounds__(kXThreads) void expand_step_kernel(XParams p) {
       if (all_ninf || won.v == -INFINITY || s_exp_cum[j].hi == -INFINITY) cv = DF{-INFINITY, 0.f};
       else cv = df_add(s_exp_cum[j], df_add(DF{won.v, 0.f}, df_neg(lse)));
       c_cum[sl] = cv;
-      c_key[sl] = df_key(cv);
+      u_key[P + sl] = df_key(cv);
       c_token[sl] = p.token_map ? p.token_map[won.i] : won.i;
       c_parent[sl] = s_exp_node[j];
       c_depth[sl] = s_exp_depth[j] + 1;
-      c_order[sl] = s_gen + sl;
+      u_ord[P + sl] = s_gen + sl;
     }
     if (lane == 0) s_count[j] = nvalid;
     __syncwarp();
@@ -623,31 +621,35 @@ __global__ __launch_bounds__(kXThreads) void expand_step_kernel(XParams p) {
   if (pops > total) pops = total;
   __shared__ DF n_cum[kXN];
   __shared__ int n_parent[kXN], n_token[kXN], n_depth[kXN], n_order[kXN];
-  for (int t = tid; t < P + E * K; t += blockDim.x) {
+  // rank of slot u = the valid slots that precede it, counted by S threads
+  // of one warp that scan every S-th slot (all threads of a warp read the
+  // same or neighbouring slots: broadcasts, no dependent load chains)
+  const int nslot = P + E * K;
+  int S = 1;
+  while (S < 32 && 2 * S * nslot <= kXThreads) S <<= 1;
+  const int per = kXThreads / S, sub = tid & (S - 1);
+  for (int base = 0; base < nslot; base += per) {   // uniform trip count: the shuffles below see whole warps
+    const int u = base + tid / S;
+    const bool live = u < nslot;
+    const uint64_t kk = live ? u_key[u] : 0;
+    const int o = live ? u_ord[u] : kXNoOrder;
+    int rank = 0;
+    if (o != kXNoOrder)
+      for (int v = sub; v < nslot; v += S) rank += cand_before(u_key[v], u_ord[v], kk, o);
+    for (int off = 1; off < S; off <<= 1) rank += __shfl_xor_sync(0xffffffffu, rank, off);
+    if (o == kXNoOrder || sub != 0) continue;
     DF c;
-    uint64_t kk;
-    int o, pa, tk, dp, rank;
-    if (t < P) {
-      c = q_cum[t];
-      kk = q_key[t];
-      o = q_order[t];
-      pa = q_parent[t];
-      tk = q_token[t];
-      dp = q_depth[t];
-      rank = t;
-      for (int j = 0; j < E; ++j) rank += count_before(c_key + j * K, c_order + j * K, s_count[j], kk, o);
+    int pa, tk, dp;
+    if (u < P) {
+      c = q_cum[u];
+      pa = q_parent[u];
+      tk = q_token[u];
+      dp = q_depth[u];
     } else {
-      const int sl = t - P, j = sl / K, r = sl - j * K;
-      if (r >= s_count[j]) continue;
-      c = c_cum[sl];
-      kk = c_key[sl];
-      o = c_order[sl];
-      pa = c_parent[sl];
-      tk = c_token[sl];
-      dp = c_depth[sl];
-      rank = r + count_before(q_key, q_order, P, kk, o);
-      for (int j2 = 0; j2 < E; ++j2)
-        if (j2 != j) rank += count_before(c_key + j2 * K, c_order + j2 * K, s_count[j2], kk, o);
+      c = c_cum[u - P];
+      pa = c_parent[u - P];
+      tk = c_token[u - P];
+      dp = c_depth[u - P];
     }
     if (rank < pops) {
       const int i = s_n + rank;
