@@ -227,8 +227,7 @@ __global__ __launch_bounds__(kXTopkThreads) void draft_topk_kernel(const void* _
   __shared__ int s_wi[NW];
   __shared__ float s_sum[NW], s_sum_lo[NW];
   __shared__ int s_cnt;
-  __shared__ float cv[kXCand];
-  __shared__ int ci[kXCand];
+  __shared__ uint64_t ck[kXCand];                // candidates as entry keys
   __shared__ Ent wtop[NW][KT];
   if (threadIdx.x == 0) s_cnt = 0;
   dep_wait();
@@ -283,23 +282,23 @@ __global__ __launch_bounds__(kXTopkThreads) void draft_topk_kernel(const void* _
       if (!(xv < INFINITY)) continue;            // NaN, +inf
       if (xv > -INFINITY) s += exp2f((xv - M) * kLog2e);
     }
-    // candidates (>= T), appended with one shared atomic per warp and entry slot
+    // candidates (>= T, not NaN, not +inf), appended with one shared
+    // atomic per warp and tile (ballots counted first, then recomputed)
+    int tot = 0;
+#pragma unroll
+    for (int k = 0; k < PT; ++k) tot += __popc(__ballot_sync(0xffffffffu, x[k] < INFINITY && x[k] >= T));
+    if (tot == 0) return;                        // warp-uniform
+    int base = 0;
+    if (lane == 0) base = atomicAdd(&s_cnt, tot);
+    base = __shfl_sync(0xffffffffu, base, 0);
+    const uint32_t below = (1u << lane) - 1u;
 #pragma unroll
     for (int k = 0; k < PT; ++k) {
-      const float xv = x[k];
-      const bool cand = xv < INFINITY && xv >= T;  // not NaN, not +inf
+      const bool cand = x[k] < INFINITY && x[k] >= T;
       const uint32_t m = __ballot_sync(0xffffffffu, cand);
-      if (m == 0u) continue;
-      int base = 0;
-      if (lane == __ffs(m) - 1) base = atomicAdd(&s_cnt, __popc(m));
-      base = __shfl_sync(0xffffffffu, base, __ffs(m) - 1);
-      if (cand) {
-        const int pos = base + __popc(m & ((1u << lane) - 1u));
-        if (pos < kXCand) {
-          cv[pos] = xv;
-          ci[pos] = tile_index<BF16>(t0, k, vec);
-        }
-      }
+      const int pos = base + __popc(m & below);
+      if (cand && pos < kXCand) ck[pos] = ent_key(x[k], tile_index<BF16>(t0, k, vec));
+      base += __popc(m);
     }
   };
   if (one_tile) {
@@ -324,27 +323,26 @@ __global__ __launch_bounds__(kXTopkThreads) void draft_topk_kernel(const void* _
   float* ov = pv + slot * K;
   int32_t* oi = pi + slot * K;
   if (n <= kXCand) {
-    // warp 0: K rounds, each taking the first remaining candidate
+    // warp 0: K rounds, round r taking the largest key below round r - 1's
+    // (keys are distinct; every lane scans the same number of slots, with
+    // no branch on the data)
     if (warp == 0) {
+      uint64_t prev = ~0ull;
       int r = 0;
       for (; r < K; ++r) {
-        Ent mine{-INFINITY, -1};
-        int mu = -1;
-        for (int u = lane; u < n; u += 32) {
-          const Ent c2{cv[u], ci[u]};
-          if (ent_before(c2, mine)) {
-            mine = c2;
-            mu = u;
-          }
+        uint64_t mine = 0ull;
+        for (int u0 = 0; u0 < n; u0 += 32) {
+          const uint64_t k2 = u0 + lane < n ? ck[u0 + lane] : 0ull;
+          mine = (k2 < prev && k2 > mine) ? k2 : mine;
         }
-        const Ent best = warp_first(mine);
-        if (best.i < 0) break;                     // fewer than K candidates
-        if (mine.i == best.i) ci[mu] = -1;         // taken
+        const uint64_t w = warp_max_key(mine);
+        if (w == 0ull) break;                      // fewer than K candidates
+        prev = w;
         if (lane == 0) {
+          const Ent best = key_ent(w);
           ov[r] = best.v;
           oi[r] = best.i;
         }
-        __syncwarp();
       }
       for (int r2 = r + lane; r2 < K; r2 += 32) {
         ov[r2] = -INFINITY;
@@ -380,7 +378,7 @@ __global__ __launch_bounds__(kXTopkThreads) void draft_topk_kernel(const void* _
       }
     }
   }
-  if (warp == 0) {
+  if (warp == 1) {                               // beside warp 0's rounds
     DF S = lane < NW ? DF{s_sum[lane], s_sum_lo[lane]} : DF{0.f, 0.f};
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
@@ -534,40 +532,44 @@ __global__ __launch_bounds__(kXThreads) void expand_step_kernel(XParams p) {
 
   // children of each expanded row (warp j % NW): the row's log-sum-exp from
   // its chunks, and its top-K by K rounds over the heads of the chunks'
-  // sorted lists (staged in shared memory with one round of loads)
-  __shared__ float w_v[NW][kXRowEntries];
-  __shared__ int w_i[NW][kXRowEntries];
+  // sorted lists (staged in shared memory as entry keys)
+  constexpr int RE = kXRowEntries / 32;
+  __shared__ uint64_t w_k[NW][kXRowEntries];
   const int vc = p.vchunks, nE = vc * K;
   for (int j = warp; j < E; j += NW) {
     if (s_exp_depth[j] >= p.max_depth) continue;   // at the depth limit: no children
     const int64_t row = (int64_t)b * p.R + j;
     const float* rv = p.pv + row * nE;
     const int32_t* ri = p.pi + row * nE;
-    for (int t = lane; t < nE; t += 32) {
-      w_v[warp][t] = rv[t];
-      w_i[warp][t] = ri[t];
+    // every load of the row in one round: the lists, then the chunks'
+    // maxima and sums (chunks lane and lane + 32)
+    float lv[RE];
+    int li[RE];
+#pragma unroll
+    for (int q = 0; q < RE; ++q) {
+      const int t = lane + 32 * q;
+      lv[q] = t < nE ? __ldcg(rv + t) : -INFINITY;
+      li[q] = t < nE ? __ldcg(ri + t) : -1;
     }
-    float M = -INFINITY;
-    bool bad = false;
-    for (int cc = lane; cc < vc; cc += 32) {
-      const float mc = p.pm[row * vc + cc];
-      bad |= mc == INFINITY;
-      if (mc != INFINITY) M = fmaxf(M, mc);
+    const float mc0 = lane < vc ? __ldcg(p.pm + row * vc + lane) : -INFINITY;
+    const float mc1 = lane + 32 < vc ? __ldcg(p.pm + row * vc + lane + 32) : -INFINITY;
+    const float2 sc0 = lane < vc ? __ldcg(p.ps + row * vc + lane) : make_float2(0.f, 0.f);
+    const float2 sc1 = lane + 32 < vc ? __ldcg(p.ps + row * vc + lane + 32) : make_float2(0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < RE; ++q) {
+      const int t = lane + 32 * q;
+      if (t < nE) w_k[warp][t] = li[q] < 0 ? 0ull : ent_key(lv[q], li[q]);
     }
-    if (__any_sync(0xffffffffu, bad)) {
+    if (__any_sync(0xffffffffu, mc0 == INFINITY || mc1 == INFINITY)) {
       if (lane == 0) set_status(p.status, TV_DEV_BAD_LOGITS);
       continue;
     }
+    float M = fmaxf(mc0, mc1);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     DF S{0.f, 0.f};
-    for (int cc = lane; cc < vc; cc += 32) {
-      const float mc = p.pm[row * vc + cc];
-      if (mc > -INFINITY) {
-        const float2 sc = p.ps[row * vc + cc];
-        S = df_add(S, df_mulf(DF{sc.x, sc.y}, exp2f((mc - M) * kLog2e)));
-      }
-    }
+    if (mc0 > -INFINITY) S = df_add(S, df_mulf(DF{sc0.x, sc0.y}, exp2f((mc0 - M) * kLog2e)));
+    if (mc1 > -INFINITY) S = df_add(S, df_mulf(DF{sc1.x, sc1.y}, exp2f((mc1 - M) * kLog2e)));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
       S = df_add(S, DF{__shfl_xor_sync(0xffffffffu, S.hi, off), __shfl_xor_sync(0xffffffffu, S.lo, off)});
@@ -575,34 +577,44 @@ __global__ __launch_bounds__(kXThreads) void expand_step_kernel(XParams p) {
     const bool all_ninf = !(M > -INFINITY);
     const DF lse = all_ninf ? DF{-INFINITY, 0.f} : df_add(DF{M, 0.f}, df_log_ge1(S));
     __syncwarp();
-    // lane l walks the lists of chunks l and l + 32; lane r keeps the r-th
-    // winner
-    int q0 = 0, q1 = 0;
+    // lane l walks the lists of chunks l and l + 32 (head h, next entry n,
+    // loaded a round ahead); lane r keeps the r-th winner
+    const bool has0 = lane < vc, has1 = lane + 32 < vc;
+    const uint64_t* L0 = &w_k[warp][has0 ? lane * K : 0];
+    const uint64_t* L1 = &w_k[warp][has1 ? (lane + 32) * K : 0];
+    uint64_t h0 = has0 ? L0[0] : 0ull, n0 = has0 && K > 1 ? L0[1] : 0ull;
+    uint64_t h1 = has1 ? L1[0] : 0ull, n1 = has1 && K > 1 ? L1[1] : 0ull;
+    int q0 = 1, q1 = 1;                            // index of the next entry
     int nvalid = 0;
-    Ent won{-INFINITY, -1};                        // lane r keeps the r-th winner
+    uint64_t won = 0ull;
     for (int r = 0; r < K; ++r) {
-      const int c0 = lane, c1 = lane + 32;
-      const Ent h0 = (c0 < vc && q0 < K) ? Ent{w_v[warp][c0 * K + q0], w_i[warp][c0 * K + q0]} : Ent{-INFINITY, -1};
-      const Ent h1 = (c1 < vc && q1 < K) ? Ent{w_v[warp][c1 * K + q1], w_i[warp][c1 * K + q1]} : Ent{-INFINITY, -1};
-      const Ent h = ent_before(h1, h0) ? h1 : h0;
-      const Ent best = warp_first(h);
-      if (best.i < 0) break;                       // the row has no more valid entries
-      if (h0.i == best.i) ++q0;
-      else if (h1.i == best.i) ++q1;
-      if (lane == r) won = best;
+      const uint64_t w = warp_max_key(h0 > h1 ? h0 : h1);
+      if (w == 0ull) break;                        // warp-uniform: the row has no more valid entries
+      won = lane == r ? w : won;
       nvalid = r + 1;
+      // the lane holding w advances that list (selects, no branch; the
+      // loads read a clamped, always valid slot)
+      const bool a0 = h0 == w, a1 = !a0 && h1 == w;
+      q0 += a0;
+      q1 += a1;
+      const uint64_t f0 = L0[q0 < K ? q0 : K - 1], f1 = L1[q1 < K ? q1 : K - 1];
+      h0 = a0 ? n0 : h0;
+      h1 = a1 ? n1 : h1;
+      n0 = a0 ? (q0 < K ? f0 : 0ull) : n0;
+      n1 = a1 ? (q1 < K ? f1 : 0ull) : n1;
     }
     // the children, one per lane: cumulative log-probability = parent's +
     // (logit - lse); -inf when the row (or the logit, or the parent) has
     // probability 0
     if (lane < nvalid) {
+      const Ent e = key_ent(won);
       const int sl = j * K + lane;
       DF cv;
-      if (all_ninf || won.v == -INFINITY || s_exp_cum[j].hi == -INFINITY) cv = DF{-INFINITY, 0.f};
-      else cv = df_add(s_exp_cum[j], df_add(DF{won.v, 0.f}, df_neg(lse)));
+      if (all_ninf || e.v == -INFINITY || s_exp_cum[j].hi == -INFINITY) cv = DF{-INFINITY, 0.f};
+      else cv = df_add(s_exp_cum[j], df_add(DF{e.v, 0.f}, df_neg(lse)));
       c_cum[sl] = cv;
       u_key[P + sl] = df_key(cv);
-      c_token[sl] = p.token_map ? p.token_map[won.i] : won.i;
+      c_token[sl] = p.token_map ? p.token_map[e.i] : e.i;
       c_parent[sl] = s_exp_node[j];
       c_depth[sl] = s_exp_depth[j] + 1;
       u_ord[P + sl] = s_gen + sl;

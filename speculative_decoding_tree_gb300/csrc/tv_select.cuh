@@ -46,4 +46,23 @@ __device__ __forceinline__ Ent warp_first(Ent e) {
   return best == 0u ? Ent{-INFINITY, -1} : Ent{key_val(best), (int)bi};
 }
 
+// The same order as one 64-bit integer (larger = first): the value key
+// above, then the complemented index (smaller index = larger).  A valid
+// entry's key is nonzero; 0 is the empty entry.
+__device__ __forceinline__ uint64_t ent_key(float v, int i) {
+  return ((uint64_t)val_key(v) << 32) | (uint32_t)~i;
+}
+
+__device__ __forceinline__ Ent key_ent(uint64_t k) {
+  return k == 0ull ? Ent{-INFINITY, -1} : Ent{key_val((uint32_t)(k >> 32)), (int)~(uint32_t)k};
+}
+
+// The warp's largest 64-bit key (two reductions: high word, then the low
+// word among the lanes holding that high word).
+__device__ __forceinline__ uint64_t warp_max_key(uint64_t k) {
+  const uint32_t hi = __reduce_max_sync(0xffffffffu, (uint32_t)(k >> 32));
+  const uint32_t lo = __reduce_max_sync(0xffffffffu, (uint32_t)(k >> 32) == hi ? (uint32_t)k : 0u);
+  return ((uint64_t)hi << 32) | lo;
+}
+
 }  // namespace tv
