@@ -39,6 +39,11 @@ using namespace tc;
 constexpr int BM = 128;                         // query rows per CTA
 constexpr int BN = 128;                         // keys per tile
 constexpr int KH = 64;                          // keys per CTA in a K half
+// key tiles of the chunk warmed in L2 before the dependency wait (measured on
+// the 4K, 32K and batched workloads: 2 beats 1, 4 and 8 by up to 7%; warming
+// further tiles while streaming was slower, up to 35% on the batched one)
+constexpr int kPrefetchTiles = 2;
+static_assert(kPrefetchTiles >= 0 && kPrefetchTiles <= 32, "one lane per prefetched tile");
 constexpr uint64_t kWaitNs = 1000000000ull;
 constexpr float kRescaleThreshold = 8.0f;       // rescale O when the max grows by > 2^8
 constexpr int kThreads = 384;
@@ -153,24 +158,48 @@ tv_attn_tc2_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   cluster_sync_all();                               // both CTAs' barriers exist before any remote use
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (warp == 3 && lane == 0) {
+  if (warp == 3) {
     // an idle warp warms L2 (and the TLB) for what the first steps read,
-    // while the previous kernel may still run: the sequence's lengths,
-    // this CTA's half of the first K and V tiles of its chunk (contiguous
-    // cache) and, for the first sequence (rows start at 0), its query tile
+    // while the previous kernel may still run: the sequence's lengths, this
+    // CTA's halves of the first kPrefetchTiles K and V tiles its chunk can
+    // hold (bounded by the host's max_prefix, since the length itself is
+    // not read yet) and, for the first sequence (rows start at 0), its query
+    // tile.  These are hints: a prefetch has no effect on memory ordering,
+    // so a line the previous kernel writes later is still read fresh, and a
+    // page id read here only picks which lines to warm (a stale or invalid
+    // id costs a wasted prefetch, never a wrong value).
     const int b = blockIdx.z, g = blockIdx.y / p.splits, s = blockIdx.y % p.splits;
     const uint32_t rank = cluster_ctarank();
-    prefetch_l2(p.prefix_len + b);
-    prefetch_l2(p.node_offsets + b);
+    const int64_t c0 = (int64_t)s * p.chunk;
+    const int64_t c1 = min(p.max_prefix, c0 + p.chunk);
+    const int npf = c1 > c0 ? (int)min((int64_t)kPrefetchTiles, (c1 - c0 + BN - 1) / BN) : 0;
+    if (lane == 0) {
+      prefetch_l2(p.prefix_len + b);
+      prefetch_l2(p.node_offsets + b);
+      if (b == 0)
+        for (int kb = 0; kb < D / 64; ++kb) tma_prefetch_3d(&tm_q, kb * 64, g * p.G, blockIdx.x * p.rows_per_tile / p.G);
+    }
     if (!p.paged) {
-      const int64_t row = ((int64_t)b * p.Hkv + g) * p.capacity + (int64_t)s * p.chunk;
-      if (row + BN <= (int64_t)INT_MAX) {
+      const int64_t row = ((int64_t)b * p.Hkv + g) * p.capacity + c0 + (int64_t)lane * BN;   // lane = tile
+      if (lane < npf && row + BN <= (int64_t)INT_MAX) {
         for (int bx = 0; bx < D / 64; ++bx) tma_prefetch_2d(&tm_kc, bx * 64, (int)row + KH * (int)rank);
         for (int bx = 0; bx < D / 128; ++bx) tma_prefetch_2d(&tm_vc, (D / 2) * (int)rank + bx * 64, (int)row);
       }
+    } else {
+      // pages of the first tiles that hold keys below c1 (c1 <= capacity, so every index
+      // stays inside the sequence's row of the page table)
+      const int npg = (int)min((int64_t)npf * (BN / kPageSize), (c1 - c0 + kPageSize - 1) / kPageSize);
+      for (int pg = lane; pg < npg; pg += 32) {
+        const int64_t pos = c0 + (int64_t)pg * kPageSize;
+        const int pid = p.page_table[(int64_t)b * p.max_pages + pos / kPageSize];
+        if (pid >= 0 && pid < p.num_pages) {
+          const int row = (int)(((int64_t)pid * p.Hkv + g) * kPageSize);
+          if ((pg % (BN / kPageSize)) / (KH / kPageSize) == (int)rank)   // a page of this CTA's K half
+            for (int bx = 0; bx < D / 64; ++bx) tma_prefetch_2d(&tm_kc, bx * 64, row);
+          for (int bx = 0; bx < D / 128; ++bx) tma_prefetch_2d(&tm_vc, (D / 2) * (int)rank + bx * 64, row);
+        }
+      }
     }
-    if (b == 0)
-      for (int kb = 0; kb < D / 64; ++kb) tma_prefetch_3d(&tm_q, kb * 64, g * p.G, blockIdx.x * p.rows_per_tile / p.G);
   }
   dep_wait();
   dep_launch();
