@@ -22,16 +22,20 @@ int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 }  // namespace
 
 int num_sms() {
-  static int cached = 0;
-  if (cached > 0) return cached;
+  // per device (plans are made for the current device), safe across host threads
+  static std::atomic<int> cached[kAttrDevices];
   int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) == cudaSuccess &&
-      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0) {
-    cached = n;
-  } else {
+  if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();  // clear the error left by a machine without a GPU
-    n = kNumSMsDefault;
+    return kNumSMsDefault;
   }
+  const bool tracked = dev >= 0 && dev < kAttrDevices;
+  if (tracked && (n = cached[dev].load(std::memory_order_relaxed)) > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return kNumSMsDefault;
+  }
+  if (tracked) cached[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 

@@ -278,13 +278,8 @@ cudaError_t launch_simt_t(const AttnParams& p, cudaStream_t s) {
   constexpr int RPW = 1024 / D;
   constexpr int ROWS = 4 * RPW;
   const size_t smem = sizeof(float) * (ROWS * D + kKeyTile * (D + 4) + kKeyTile * D + 4 * RPW * kKeyTile);
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_simt_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = ensure_max_dynamic_smem<attn_simt_kernel<T, D>>((int)smem);
+  if (e != cudaSuccess) return e;
   dim3 grid(p.row_tiles * p.Hkv, p.splits, p.B);
   return launch_dep(attn_simt_kernel<T, D>, grid, dim3(128), smem, s, p);
 }

@@ -680,13 +680,8 @@ cudaError_t launch_tc_t(const AttnParams& p, cudaStream_t st) {
                 p.part_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
       return cudaErrorInvalidValue;
   }
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(tv_attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)Cfg<D>::SMEM);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = ensure_max_dynamic_smem<tv_attn_tc_kernel<D>>((int)Cfg<D>::SMEM);
+  if (e != cudaSuccess) return e;
   dim3 grid(p.row_tiles, p.Hkv * p.splits, p.B);
   return launch_dep(tv_attn_tc_kernel<D>, grid, dim3(kThreads), Cfg<D>::SMEM, st, p, mq, mkc, mvc, mkt, mvt, mop);
 }

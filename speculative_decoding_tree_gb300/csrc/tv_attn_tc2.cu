@@ -718,13 +718,8 @@ cudaError_t launch_tc2_t(const AttnParams& p, cudaStream_t st) {
                  p.part_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
       return cudaErrorInvalidValue;
   }
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(tv_attn_tc2_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)Cfg2<D>::SMEM);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = ensure_max_dynamic_smem<tv_attn_tc2_kernel<D>>((int)Cfg2<D>::SMEM);
+  if (e != cudaSuccess) return e;
   dim3 grid(2 * ((p.row_tiles + 1) / 2), p.Hkv * p.splits, p.B);
   return launch_dep(tv_attn_tc2_kernel<D>, grid, dim3(kThreads), Cfg2<D>::SMEM, st, p, mq, mkc, mvc, mkt, mvt, mop);
 }

@@ -6,6 +6,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "tree_verify.h"
 
 namespace tv {
@@ -160,6 +162,31 @@ cudaError_t launch_dep(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 // SMs of the current device (cached; a default when no device answers).
 int num_sms();
+
+// Devices whose launch attributes are tracked per device (larger ordinals set
+// the attribute on every launch).
+constexpr int kAttrDevices = 64;
+
+// Raises kernel K's dynamic shared memory limit to at least `bytes` on the
+// current device.  A function attribute belongs to a device's context, so it
+// is tracked per device: the largest size set so far, kept per kernel
+// instantiation (one static array per K).  Safe to call from several host
+// threads (setting the same attribute twice is harmless).
+template <auto K>
+cudaError_t ensure_max_dynamic_smem(int bytes) {
+  static std::atomic<int> set_bytes[kAttrDevices];   // zero-initialised
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool tracked = dev >= 0 && dev < kAttrDevices;
+  if (tracked && set_bytes[dev].load(std::memory_order_acquire) >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess || !tracked) return e;
+  int cur = set_bytes[dev].load(std::memory_order_relaxed);
+  while (cur < bytes && !set_bytes[dev].compare_exchange_weak(cur, bytes, std::memory_order_release)) {
+  }
+  return cudaSuccess;
+}
 
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_attn_simt(const AttnParams& p, int dtype, cudaStream_t s);

@@ -349,11 +349,9 @@ int tv_lm_head_argmax(const tv_lmhead_desc* desc, const void* d_hidden, const vo
   p.units = (int)(((int64_t)desc->vocab + LV - 1) / LV * p.RT);
   p.KCH = desc->hidden / LKC;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  static std::once_flag attr_once;
-  std::call_once(attr_once, [] {
-    cudaFuncSetAttribute(lmhead_argmax_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(kLSmem + 1024));
-  });
-  cudaError_t e = launch_dep(lmhead_argmax_kernel, dim3(grid), dim3(kLThreads), kLSmem + 1024, s, p, tm_w, tm_h);
+  cudaError_t e = ensure_max_dynamic_smem<lmhead_argmax_kernel>((int)(kLSmem + 1024));
+  if (e != cudaSuccess) return TV_ERR_CUDA;
+  e = launch_dep(lmhead_argmax_kernel, dim3(grid), dim3(kLThreads), kLSmem + 1024, s, p, tm_w, tm_h);
   if (e != cudaSuccess) return TV_ERR_CUDA;
   e = launch_dep(lmhead_finish_kernel, dim3((desc->rows + 7) / 8), dim3(256), 0, s, (const float*)p.part_v,
                  (const int32_t*)p.part_i, grid, desc->rows, d_argmax, d_max_logit);

@@ -199,13 +199,8 @@ __global__ __launch_bounds__(kMergeThreads) void merge_slab_kernel(MergeParams p
 template <int D, typename PT>
 cudaError_t launch_merge_t(const MergeParams& p, cudaStream_t s) {
   const size_t smem = (size_t)p.batch_splits * p.slab_rows * (D * sizeof(PT) + 8 + 4);
-  static size_t configured = 0;
-  if (smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(merge_slab_kernel<D, PT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = smem;
-  }
+  cudaError_t e = ensure_max_dynamic_smem<merge_slab_kernel<D, PT>>((int)smem);
+  if (e != cudaSuccess) return e;
   dim3 grid((p.tile_stride + p.slab_rows - 1) / p.slab_rows, p.Hkv * p.row_tiles, p.B);
   return launch_dep(merge_slab_kernel<D, PT>, grid, dim3(kMergeThreads), smem, s, p);
 }

@@ -183,3 +183,30 @@ def test_bounded_wait_runs_out_and_the_context_stays_usable():
     assert int(st[0]) == 32
     w = workload(wl.small_variant(3))
     check_step(w, run(w), oracle.verify_step(w))
+
+
+@pytest.mark.parametrize("spec", [
+    wl.CONFIGS[3].replace(prefix=(2000, 2000), tree="random:48,48,6", vocab=300, p_match=0.9, seed=611,
+                          cache_margin=200),
+    wl.CONFIGS[5].replace(batch=3, prefix=(700, 2500), vocab=300, p_match=0.9, seed=612, cache_margin=200),
+], ids=["pairs-contiguous", "one-cta-paged"])
+def test_attention_right_after_commit(spec):
+    # accept + commit, then attention over the grown prefix, back to back on
+    # one stream (no host sync): the split kernel's prefetches and loads of
+    # the committed rows follow the commit kernel directly
+    w = workload(spec)
+    P0 = w.prefix_len.clone()
+    st = DeviceStep(w, max_prefix=int(P0.max()) + 64)
+    st.mask()
+    st.attn()
+    st.accept_commit()
+    st.attn()
+    torch.cuda.synchronize()
+    assert int(st.status[0].item()) == 0
+    ref = oracle.verify_step(w)
+    assert torch.equal(st.prefix_len.cpu(), ref["prefix_len"])
+    w2 = workload(spec)
+    w2.k_cache, w2.v_cache, w2.prefix_len = ref["k_cache"], ref["v_cache"], ref["prefix_len"].clone()
+    ref2 = oracle.verify_step(w2)
+    err = np.abs(st.out.double().cpu().numpy() - ref2["out"]).max()
+    assert err <= TOL[w.spec.dtype], err
