@@ -88,7 +88,9 @@ enum {
   TV_ERR_HEAD_DIM = -3,    /* head_dim not 128, 256 or 512 */
   TV_ERR_ZERO_HEADS = -4,  /* num_q_heads or num_kv_heads <= 0 (checked before the modulo) */
   TV_ERR_GQA = -5,         /* num_q_heads % num_kv_heads != 0 */
-  TV_ERR_SHAPE = -6,       /* batch, total_rows, vocab, capacity or max_prefix out of range */
+  TV_ERR_SHAPE = -6,       /* batch, total_rows, vocab, capacity or max_prefix out of range, or a launch
+                              grid extent above 65535: batch, KV heads x splits, KV heads x row tiles,
+                              or total_rows for acceptance */
   TV_ERR_TREE = -7,        /* max_nodes outside 1..64, or total_rows outside batch..batch*max_nodes */
   TV_ERR_PAGED = -8,       /* page_size not 0 or 16, capacity not a multiple of 16, or no pages */
   TV_ERR_OVERFLOW = -9,    /* a byte count overflows int64 */

@@ -128,6 +128,11 @@ int make_plan(const tv_desc* d, Plan* p) {
   int splits = num_chunks(L, (int)chunk, tree_tile);
   int64_t grid = units * splits;
   if (grid > ((int64_t)1 << 31) - 1) return TV_ERR_OVERFLOW;
+  // launch grids put sequences on z and (KV head, split) or (KV head, row
+  // tile) on y, whose limit is 65535: refused here rather than at launch
+  const int64_t grid_y = tc ? (int64_t)d->num_kv_heads * splits : (int64_t)splits;
+  if (d->batch > kMaxGridYZ || grid_y > kMaxGridYZ || (int64_t)d->num_kv_heads * row_tiles > kMaxGridYZ)
+    return TV_ERR_SHAPE;
   p->G = G;
   p->tree_tile = tree_tile;
   p->pub.kernel = pairs ? 2 : (tc ? 1 : 0);
@@ -264,6 +269,7 @@ int accept_commit_impl(const tv_desc* desc, int32_t vocab, int32_t logits_dtype,
                        void* stream) {
   int rc = validate(desc);
   if (rc) return rc;
+  if (desc->total_rows > kMaxGridYZ) return TV_ERR_SHAPE;   // one argmax row per grid y index
   if (logits_dtype != TV_F32 && logits_dtype != TV_BF16) return TV_ERR_DTYPE;
   if (vocab < 1) return TV_ERR_SHAPE;
   if (!d_logits || !d_draft_tokens || !d_parents || !d_node_offsets || !d_k_tree || !d_v_tree || !d_k_cache ||

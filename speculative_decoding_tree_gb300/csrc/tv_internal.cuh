@@ -16,6 +16,7 @@ constexpr int kPageSize = 16;
 constexpr int kMaxNodes = 64;
 constexpr int kNumSMsDefault = 148;
 constexpr int kMaxVChunks = 32;      // vocabulary chunks per row in the argmax pass
+constexpr int64_t kMaxGridYZ = 65535;   // CUDA's limit on a launch grid's y and z extents
 
 // Everything the split-KV attention kernels read, resolved on the host.
 struct AttnParams {

@@ -72,6 +72,29 @@ def test_descriptor_validation(L, kw, code):
     assert rc == code
 
 
+def test_grid_limits_refused_on_the_host(L):
+    # launch grids keep sequences on z and (KV head, split) on y: extents
+    # above 65535 are refused before any launch, not by the driver
+    n = ctypes.c_size_t(0)
+    fake = 1 << 20
+    big_batch = _desc(batch=70000, total_rows=70000, max_nodes=1, capacity=64, max_prefix=64)
+    assert L.tv_workspace_size(ctypes.byref(big_batch), 0, ctypes.byref(n)) == -6
+    assert L.tree_verify_attn(ctypes.byref(big_batch), *([fake] * 10), fake, 1 << 30, fake, None) == -6
+    # 64 KV heads x 1100 chunks of 2048 keys on the tensor-core kernel (16 rows per KV head)
+    many_splits = _desc(batch=2, num_q_heads=256, num_kv_heads=64, head_dim=128, max_nodes=4, total_rows=8,
+                        capacity=2048 * 1100, max_prefix=2048 * 1100)
+    assert tv.tv_attn_plan(_desc(batch=2, num_q_heads=256, num_kv_heads=64, head_dim=128, max_nodes=4,
+                                 total_rows=8, capacity=2048 * 1000, max_prefix=2048 * 1000))["kernel"] == 1
+    assert L.tv_workspace_size(ctypes.byref(many_splits), 0, ctypes.byref(n)) == -6
+    ok_splits = _desc(batch=2, num_q_heads=256, num_kv_heads=64, head_dim=128, max_nodes=4, total_rows=8,
+                      capacity=2048 * 1000, max_prefix=2048 * 1000)
+    assert L.tv_workspace_size(ctypes.byref(ok_splits), 0, ctypes.byref(n)) == 0
+    many_rows = _desc(batch=2000, max_nodes=64, total_rows=66000, capacity=64, max_prefix=32)
+    assert L.tv_workspace_size(ctypes.byref(many_rows), 0, ctypes.byref(n)) == 0   # attention alone is fine
+    args = [fake] * 15
+    assert L.tree_accept_commit(ctypes.byref(many_rows), 1000, 1, *args, 1 << 30, fake, None) == -6
+
+
 def test_null_and_alignment_and_workspace(L):
     d = _desc()
     fake = 1 << 20
