@@ -191,9 +191,7 @@ def make_sets(spec, device):
 
     sets = []
     w0 = wl.make_workload(spec, canary=0.0, argmax_fn=argmax_cpu)
-    per_set = (w0.k_cache.numel() * w0.k_cache.element_size() * 2 + w0.logits.numel() * w0.logits.element_size()
-               + w0.q.numel() * w0.q.element_size() * 2)
-    nsets = max(2, math.ceil(3 * L2_BYTES / per_set))
+    per_set, nsets, _ = set_layout(w0)
     for i in range(nsets):
         w = w0 if i == 0 else wl.make_workload(spec.replace(seed=spec.seed + 7919 * i), canary=0.0,
                                                argmax_fn=argmax_cpu)
@@ -350,83 +348,89 @@ def lm_head_timing(cap_stream, peak, reps=5, calls=6):
     return out
 
 
-def run_ours(args, ws, rank):
-    import numpy as np  # noqa: F401
-    from speculative_decoding_tree_gb300 import _build
-    _build.build()
-    import speculative_decoding_tree_gb300 as tv
+def bench_config(spec, w, nsets, per_set, per_big, ws):
+    """The workload description both arms print (the reference arm times the
+    oracle on the same workload and prints the same dict)."""
+    return {
+        "workload": spec.name, "batch": spec.batch, "q_heads": spec.hq, "kv_heads": spec.hkv,
+        "head_dim": spec.d, "prefix": list(spec.prefix), "tree_rows": int(w.total_rows), "vocab": spec.vocab,
+        "paged": spec.paged, "parallelism": "replicas" if ws > 1 else "single",
+        "l2": f"inputs rotate over {nsets} copies ({nsets * per_set / 1e6:.0f} MB > 129 MB L2)",
+        "timing": f"CUDA-graph replays of {per_big} whole steps per graph (the remainder one per graph), CUDA events",
+    }
 
-    device = torch.device("cuda", torch.cuda.current_device())
-    spec = wl.CONFIGS[args.config]
-    sets, per_set = make_sets(spec, device)
-    nsets = len(sets)
-    w = sets[0].w
-    rows = w.total_rows
-    stream = torch.cuda.current_stream()
 
+def set_layout(w):
+    """Bytes of one input set and how many sets the rotation needs so that a
+    step's inputs are not in L2 when it starts."""
+    per_set = (w.k_cache.numel() * w.k_cache.element_size() * 2 + w.logits.numel() * w.logits.element_size()
+               + w.q.numel() * w.q.element_size() * 2)
+    nsets = max(2, math.ceil(3 * L2_BYTES / per_set))
+    return per_set, nsets, nsets * max(1, math.ceil(8 / nsets))
+
+
+class Harness:
+    """One workload's rotating device input sets, the step graphs and the
+    back-to-back per-call timing."""
+
+    def __init__(self, spec, device, cap_stream, warmup):
+        self.spec = spec
+        self.cap_stream = cap_stream
+        self.sets, self.per_set = make_sets(spec, device)
+        self.nsets = len(self.sets)
+        self.w = self.sets[0].w
+        self.rows = self.w.total_rows
+        for i in range(max(warmup, 3)):
+            self.step(self.sets[i % self.nsets])
+        torch.cuda.synchronize()
+        self.graphs = []
+        for st in self.sets:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap_stream):
+                self.step(st)
+            self.graphs.append(g)
+        # whole rotations over the input sets in one graph (at least 8 steps),
+        # so that graph launches do not sit between every two steps; every
+        # step in it does all of its work
+        self.per_big = self.nsets * max(1, math.ceil(8 / self.nsets))
+        self.big = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.big, stream=cap_stream):
+            for i in range(self.per_big):
+                self.step(self.sets[i % self.nsets])
+        for i in range(max(warmup, 3)):
+            self.graphs[i % self.nsets].replay()
+        self.big.replay()
+        torch.cuda.synchronize()
+        for st in self.sets:
+            st.status.zero_()
+
+    @staticmethod
     def step(st):
         st.prefix_len.copy_(st.p0, non_blocking=True)
         st.step()
 
-    # warm-up (eager), then one CUDA graph per input set
-    for i in range(max(args.warmup, 3)):
-        step(sets[i % nsets])
-    torch.cuda.synchronize()
-    graphs = []
-    cap_stream = torch.cuda.Stream()
-    for st in sets:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=cap_stream):
-            step(st)
-        graphs.append(g)
-    # whole rotations over the input sets in one graph (at least 8 steps), so
-    # that graph launches do not sit between every two steps; every step in it
-    # does all of its work
-    per_big = nsets * max(1, math.ceil(8 / nsets))
-    big = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(big, stream=cap_stream):
-        for i in range(per_big):
-            step(sets[i % nsets])
-    for i in range(max(args.warmup, 3)):
-        graphs[i % nsets].replay()
-    big.replay()
-    torch.cuda.synchronize()
-
-    def run_steps(k):
+    def run_steps(self, k):
         """exactly k steps: whole big graphs, then single-step graphs"""
-        for _ in range(k // per_big):
-            big.replay()
-        for i in range(k % per_big):
-            graphs[i % nsets].replay()
-    for st in sets:
-        st.status.zero_()
+        for _ in range(k // self.per_big):
+            self.big.replay()
+        for i in range(k % self.per_big):
+            self.graphs[i % self.nsets].replay()
 
-    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
-    # settle the clocks under load (untimed), then the timed region
-    t_end = time.time() + 1.0
-    while time.time() < t_end:
-        run_steps(8 * per_big)
+    def time_steps(self, k):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(10_000_000)        # let the queue run ahead of the GPU
+        e0.record()
+        self.run_steps(k)
+        e1.record()
         torch.cuda.synchronize()
-    torch.cuda.synchronize()
-    barrier(ws)
-    torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda._sleep(10_000_000)        # let the queue run ahead of the GPU
-    ev0.record()
-    run_steps(args.steps)
-    ev1.record()
-    torch.cuda.synchronize()
-    barrier(ws)
-    torch.cuda.synchronize()
-    elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), ws)
+        return e0.elapsed_time(e1)
 
-    # per-kernel durations: K back-to-back launches of one call in one CUDA
-    # graph, rotating over the input sets, bracketed by two events; the
-    # per-launch time is the total over K (gaps between launches included).
-    # Every split launch reads more than L2 holds since its set was last read.
-    def b2b_us(calls, reps=5):
+    def b2b_us(self, calls, reps=5):
+        """K back-to-back launches of one call in one CUDA graph, bracketed by
+        two events; the per-launch time is the total over K (gaps between
+        launches included)."""
         g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=cap_stream):
+        with torch.cuda.graph(g, stream=self.cap_stream):
             for c in calls:
                 c()
         g.replay()
@@ -440,67 +444,161 @@ def run_ours(args, ws, rank):
             e1.record()
             torch.cuda.synchronize()
             out.append(e0.elapsed_time(e1) * 1e3 / len(calls))
+        del g
         return statistics.median(out)
 
-    for st_ in sets:                                  # the timed steps advanced prefix_len
-        st_.prefix_len.copy_(st_.p0)
+    def reset_prefix(self):
+        for st_ in self.sets:
+            st_.prefix_len.copy_(st_.p0)
+        torch.cuda.synchronize()
+
+    def accept_pool(self):
+        """(set, logits) pairs whose logits total more than 3x L2, so that each
+        accept+commit call reads its logits from HBM (sets keep logits of
+        their own shape: sets differ in their row count)."""
+        own = [st_.logits for st_ in self.sets]
+        pool = [(st_, st_.logits) for st_ in self.sets]
+        pool_bytes = sum(t.numel() * t.element_size() for t in own)
+        while pool_bytes < 3 * L2_BYTES:
+            st_ = self.sets[len(pool) % self.nsets]
+            pool.append((st_, st_.logits.clone()))
+            pool_bytes += st_.logits.numel() * st_.logits.element_size()
+        return own, pool
+
+    def breakdown(self, sampled=False):
+        """Per-call durations (us): mask, split pass, merge, the whole
+        tree_verify_attn call, accept + commit (and its sampled form)."""
+        self.reset_prefix()
+        n_b2b = max(24, 8 * self.nsets)
+        pick = [self.sets[i % self.nsets] for i in range(n_b2b)]
+        out = {"split": self.b2b_us([st_.partials for st_ in pick]),
+               "attn": self.b2b_us([st_.attn for st_ in pick]),
+               "mask": self.b2b_us([st_.mask for st_ in pick]),
+               "merge": self.b2b_us([st_.merge for st_ in pick])}
+        # accept + commit: the commit advances prefix_len, so each call starts
+        # from its set's original prefix (a copy node before each call)
+        own, pool = self.accept_pool()
+        acc_calls = []
+        for i in range(max(len(pool), n_b2b)):
+            st_, lg = pool[i % len(pool)]
+
+            def call(st_=st_, lg=lg):
+                st_.prefix_len.copy_(st_.p0, non_blocking=True)
+                st_.logits = lg
+                st_.accept_commit()
+            acc_calls.append(call)
+        out["accept"] = self.b2b_us(acc_calls)
+        if sampled:
+            # the same calls with sampled verification (temperature 1, fresh noise per call)
+            samp_calls = []
+            for i in range(max(len(pool), n_b2b)):
+                st_, lg = pool[i % len(pool)]
+
+                def scall(st_=st_, lg=lg, i=i):
+                    st_.prefix_len.copy_(st_.p0, non_blocking=True)
+                    st_.logits = lg
+                    st_.accept_commit_sampled(1.0, 20240601, i)
+                samp_calls.append(scall)
+            out["accept_sampled"] = self.b2b_us(samp_calls)
+        for st_, lg in zip(self.sets, own):
+            st_.logits = lg
+        del pool
+        self.reset_prefix()
+        return out
+
+    def status(self):
+        s = 0
+        for st_ in self.sets:
+            s |= int(st_.status[0].item())
+        return s
+
+
+def attn_summary(tv, h, bd, peak, peak_kind):
+    """The split kernel's roofline and the whole call's fraction for one workload."""
+    ab = algorithmic_bytes(h.w)
+    plan = tv.tv_attn_plan(h.sets[0].desc)
+    achieved = ab["split"] / (bd["split"] * 1e-6) / 1e9
+    roof = {
+        "kernel": {0: "attn_simt_kernel", 1: "tv_attn_tc_kernel", 2: "tv_attn_tc2_kernel"}[plan["kernel"]],
+        "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+        "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+        "traffic": profiled_traffic(h.spec.name),
+        "algorithmic_bytes_per_launch": ab["split"],
+    }
+    call = {"us": round(bd["attn"], 2), "gbs": round(ab["attn"] / (bd["attn"] * 1e-6) / 1e9, 1),
+            "frac": round(ab["attn"] / (bd["attn"] * 1e-6) / 1e9 / peak, 4),
+            "algorithmic_bytes": ab["attn"]}
+    return roof, call, plan
+
+
+def run_ours(args, ws, rank):
+    import numpy as np  # noqa: F401
+    from speculative_decoding_tree_gb300 import _build
+    _build.build()
+    import speculative_decoding_tree_gb300 as tv
+
+    device = torch.device("cuda", torch.cuda.current_device())
+    spec = wl.CONFIGS[args.config]
+    cap_stream = torch.cuda.Stream()
+    peak, peak_kind = measured_peaks()
+    h = Harness(spec, device, cap_stream, args.warmup)
+    w, rows, nsets = h.w, h.rows, h.nsets
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    # settle the clocks under load (untimed), then the timed region
+    t_end = time.time() + 1.0
+    while time.time() < t_end:
+        h.run_steps(8 * h.per_big)
+        torch.cuda.synchronize()
     torch.cuda.synchronize()
-    n_b2b = max(24, 8 * nsets)
-    pick = [sets[i % nsets] for i in range(n_b2b)]
-    split_us = b2b_us([st_.partials for st_ in pick])
-    attn_us = b2b_us([st_.attn for st_ in pick])      # the whole tree_verify_attn call
-    mask_us = b2b_us([st_.mask for st_ in pick])
-    merge_us = b2b_us([st_.merge for st_ in pick])
+    barrier(ws)
+    torch.cuda.synchronize()
+    elapsed_ms = h.time_steps(args.steps)
+    barrier(ws)
+    torch.cuda.synchronize()
+    elapsed_ms = max_over_ranks(elapsed_ms, ws)
 
-    # accept + commit: the commit advances prefix_len, so each call starts
-    # from its set's original prefix (a copy node before each call); the
-    # logits rotate over enough copies that they come from HBM each time
-    # (each set keeps logits of its own shape: sets differ in their row count)
-    own = [st_.logits for st_ in sets]
-    pool = [(st_, st_.logits) for st_ in sets]
-    pool_bytes = sum(t.numel() * t.element_size() for t in own)
-    while pool_bytes < 3 * L2_BYTES:
-        st_ = sets[len(pool) % nsets]
-        pool.append((st_, st_.logits.clone()))
-        pool_bytes += st_.logits.numel() * st_.logits.element_size()
-    acc_calls = []
-    for i in range(max(len(pool), n_b2b)):
-        st_, lg = pool[i % len(pool)]
+    bd = h.breakdown(sampled=True)
+    roof, call, plan = attn_summary(tv, h, bd, peak, peak_kind)
 
-        def call(st_=st_, lg=lg):
-            st_.prefix_len.copy_(st_.p0, non_blocking=True)
-            st_.logits = lg
-            st_.accept_commit()
-        acc_calls.append(call)
-    acc_us = b2b_us(acc_calls)
-    # the same calls with sampled verification (temperature 1, fresh noise per call)
-    samp_calls = []
-    for i in range(max(len(pool), n_b2b)):
-        st_, lg = pool[i % len(pool)]
+    # the other single-GPU workloads of the target, measured in the same
+    # process the same way (their own rotating input sets, step graphs and
+    # back-to-back call timings); the headline workload's entry repeats its
+    # own numbers
+    per_config = {}
+    for c in (3, 4, 5):
+        if c == args.config:
+            hc, bdc, rc, cc, pc, step_ms, k = h, bd, roof, call, plan, elapsed_ms, args.steps
+        else:
+            hc = Harness(wl.CONFIGS[c], device, cap_stream, 3)
+            k = 64
+            step_ms = hc.time_steps(k)
+            bdc = hc.breakdown()
+            rc, cc, pc = attn_summary(tv, hc, bdc, peak, peak_kind)
+        per_config[c] = {
+            "workload": hc.spec.name, "tree_rows": hc.rows, "rows_per_s": round(hc.rows * k / (step_ms / 1e3), 1),
+            "step_us": round(step_ms * 1e3 / k, 2), "split_us": round(bdc["split"], 2),
+            "merge_us": round(bdc["merge"], 2), "mask_us": round(bdc["mask"], 2),
+            "accept_commit_us": round(bdc["accept"], 2), "attn_call": cc, "roofline": rc,
+            "plan": {key: pc[key] for key in ("kernel", "num_splits", "chunk", "row_tiles", "grid_ctas")},
+            "device_status": hc.status(),
+        }
+        if hc is not h:
+            del hc
+            torch.cuda.empty_cache()
 
-        def scall(st_=st_, lg=lg, i=i):
-            st_.prefix_len.copy_(st_.p0, non_blocking=True)
-            st_.logits = lg
-            st_.accept_commit_sampled(1.0, 20240601, i)
-        samp_calls.append(scall)
-    samp_us = b2b_us(samp_calls)
-    for st_, lg in zip(sets, own):
-        st_.logits = lg
-        st_.prefix_len.copy_(st_.p0)
-    del pool
     expansion = expansion_timing(cap_stream)
-    rope_us, rope_bytes = rope_timing(sets, cap_stream, b2b_us)
-    lm_heads = lm_head_timing(cap_stream, measured_peaks()[0])
+    rope_us, rope_bytes = rope_timing(h.sets, cap_stream, h.b2b_us)
+    lm_heads = lm_head_timing(cap_stream, peak)
     timing_mode = ("back-to-back launches of each call in one CUDA graph over the rotating input sets, "
                    "programmatic dependent launch between them; per launch = events around the graph / launches")
     clocks = sampler.stop() if sampler else None
-    status = 0
-    for st_ in sets:
-        status |= int(st_.status[0].item())
+    status = h.status()
 
     # e2e through the public API with host buffers: per step copy the step's
     # inputs in from pinned memory, run the step, copy the results out
     # (rotating over the same input sets as above)
+    sets = h.sets
     names_in = ("q", "k_tree", "v_tree", "logits", "draft", "parents", "node_offsets")
     names_out = ("accept_len", "tokens", "path")
     host_in = [{k: getattr(s_, k).cpu().pin_memory() for k in names_in} for s_ in sets]
@@ -525,50 +623,35 @@ def run_ours(args, ws, rank):
         e1.record()
         torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws)
-    st = sets[0]
 
-    ab = algorithmic_bytes(w)
-    peak, peak_kind = measured_peaks()
     ms_per_step = elapsed_ms / args.steps
     value = aggregate(ws, rows, args.steps, elapsed_ms)
-    plan = tv.tv_attn_plan(st.desc)
-    achieved = ab["split"] / (split_us * 1e-6) / 1e9
+    config = bench_config(spec, w, nsets, h.per_set, h.per_big, ws)
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": "rows/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype, "data": "synthetic",
-        "config": {
-            "workload": spec.name, "batch": spec.batch, "q_heads": spec.hq, "kv_heads": spec.hkv,
-            "head_dim": spec.d, "prefix": list(spec.prefix), "tree_rows": rows, "vocab": spec.vocab,
-            "paged": spec.paged, "parallelism": "replicas" if ws > 1 else "single",
-            "l2": f"inputs rotate over {nsets} copies ({nsets * per_set / 1e6:.0f} MB > 129 MB L2)",
-            "timing": f"CUDA-graph replays of {per_big} whole steps per graph (the remainder one per graph), CUDA events",
-            "kernel_timing": timing_mode,
-        },
-        "roofline": {
-            "kernel": {0: "attn_simt_kernel", 1: "tv_attn_tc_kernel", 2: "tv_attn_tc2_kernel"}[plan["kernel"]],
-            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "peak_source": peak_kind,
-            "traffic": profiled_traffic(spec.name),
-            "algorithmic_bytes_per_launch": ab["split"],
-        },
+        "config": config,
+        "rows_timed_per_step": rows,
+        "kernel_timing": timing_mode,
+        "roofline": roof,
         "e2e": {"value": round(ws * rows * n_e2e / (e2e_ms / 1e3), 1), "unit": "rows/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": st.kernels_per_step() * args.steps,
+        "gpu_launches": h.sets[0].kernels_per_step() * args.steps,
         "clocks": clocks,
-        "breakdown_us": {"mask": round(mask_us, 2), "attn_split": round(split_us, 2),
-                         "attn_merge": round(merge_us, 2), "accept_commit": round(acc_us, 2)},
-        "attn_call": {"us": round(attn_us, 2), "gbs": round(ab["attn"] / (attn_us * 1e-6) / 1e9, 1),
-                      "frac": round(ab["attn"] / (attn_us * 1e-6) / 1e9 / peak, 4),
-                      "algorithmic_bytes": ab["attn"]},
-        "accept_commit_us": round(acc_us, 2),
-        "accept_commit_sampled_us": round(samp_us, 2),
+        "breakdown_us": {"mask": round(bd["mask"], 2), "attn_split": round(bd["split"], 2),
+                         "attn_merge": round(bd["merge"], 2), "accept_commit": round(bd["accept"], 2)},
+        "attn_call": call,
+        "accept_commit_us": round(bd["accept"], 2),
+        "accept_commit_sampled_us": round(bd["accept_sampled"], 2),
+        "per_config": {str(c): v for c, v in per_config.items()},
         "rope_scatter": {"us": round(rope_us, 2), "algorithmic_bytes": rope_bytes,
                          "gbs": round(rope_bytes / (rope_us * 1e-6) / 1e9, 1), "launches": 1},
         "expansion": expansion,
         "lm_head_argmax": lm_heads,
         "plan": plan,
-        "device_status": status | max(e["device_status"] for e in list(expansion.values()) + list(lm_heads.values())),
+        "device_status": status | max(e["device_status"] for e in list(expansion.values()) + list(lm_heads.values()))
+                         | max(e["device_status"] for e in per_config.values()),
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(spec, args.cpu_seconds)
@@ -620,7 +703,10 @@ def run_reference(args, ws, rank):
     t = time.perf_counter()
     oracle_sample_step(w, 1)
     one = max(time.perf_counter() - t, 1e-4)
-    budget = 90.0 / max(1, args.steps + args.warmup)
+    # every tree row per step when the whole run fits about four minutes of
+    # host time, else the same bounded sample of rows in every step
+    steps_all = args.steps + args.warmup
+    budget = 240.0 / max(1, steps_all)
     rows = max(1, min(w.total_rows, int(budget / one)))
     for _ in range(args.warmup):
         oracle_sample_step(w, rows)
@@ -631,12 +717,14 @@ def run_reference(args, ws, rank):
     value = rows * args.steps / dt
     sample = (f"each step: {rows} of {w.total_rows} tree rows (all heads) through the float64 oracle, "
               f"their argmax, acceptance and commit")
+    per_set, nsets, per_big = set_layout(w)
+    config = bench_config(spec, w, nsets, per_set, per_big, ws)
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "rows/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": spec.name, "batch": spec.batch, "q_heads": spec.hq, "kv_heads": spec.hkv,
-                   "head_dim": spec.d, "prefix": list(spec.prefix), "vocab": spec.vocab},
+        "config": config,
+        "rows_timed_per_step": rows,
         "cpu_baseline": {"value": round(value, 3), "unit": "rows/s", "cores": _CORES, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 3), "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

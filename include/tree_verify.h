@@ -304,11 +304,17 @@ int tree_accept_commit_argmax(const tv_desc* desc, const int32_t* d_argmax, cons
  * - Returns TV_ERR_WORKSPACE, enqueuing nothing, when the descriptor needs
  *   more partials than the array holds (tv_workspace_size(desc, 0) above
  *   TV_NOALLOC_SCRATCH_BYTES).
- * - The first call on a device looks up the array's device address with
- *   that device current (the caller's current device; `stream` must belong
- *   to it) and keeps it; make that first call before any stream capture.
- *   TV_ERR_CUDA if the lookup fails.
- * - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ * - Every call looks up the array's device address in the caller's current
+ *   context (`stream` must belong to that device); TV_ERR_CUDA if the lookup
+ *   fails.  The address is not kept between calls, so a context torn down
+ *   and made again (cudaDeviceReset) is handled.
+ * - The first call on each device loads this part of the library's device
+ *   code (CUDA loads modules lazily by default): that is when the driver
+ *   reserves the 32 MiB array, and the load may synchronise the device.
+ *   Warm up with one call (or one tv_workspace_size plus one call) before a
+ *   loop that must not synchronise, and before any stream capture.
+ * - Allocates nothing itself: no cudaMalloc, cudaFree or allocating library
+ *   call.
  * - Every call shares the one array and it keeps the last call's contents;
  *   nothing in it needs to start at zero (each call writes every partial it
  *   reads).  Calls whose kernels overlap on the GPU (other streams, other

@@ -25,6 +25,9 @@ and E4b.10a, §4 Phase E4):
   step, then the child's top-K rank).  With W = 1 this is the pages' global
   best-first expansion, in which a grandchild of A can enter the tree before
   a sibling of A.
+* a drafter row holding +inf is outside the log-softmax's domain: that node
+  gets no children, the rest of the expansion goes on, and the result says so
+  (`bad_logits`).
 
 The drafter is the caller's: `logits_of(step, j, path)` returns the draft
 logits of the j-th node expanded at `step` (step 0 expands the root), whose
@@ -93,6 +96,7 @@ def expand_tree(logits_of, root_token, k, n_max, width, max_depth, token_map=Non
     order = 0
     expand = [0]
     gaps = []
+    bad_logits = False
     step = 0
     while True:
         # expand the nodes moved in last step (step 0: the root)
@@ -101,6 +105,11 @@ def expand_tree(logits_of, root_token, k, n_max, width, max_depth, token_map=Non
                 continue
             path = _path(u, tokens, parents)
             row = logits_of(step, j, path)
+            if np.isposinf(_f64(row)).any():
+                # a +inf logit is outside the log-softmax's domain: the node
+                # gets no children and the expansion reports it
+                bad_logits = True
+                continue
             lp = log_softmax_row(row)
             for rank, v in enumerate(topk_row(row, k)):
                 tok = int(token_map[v]) if token_map is not None else int(v)
@@ -120,7 +129,8 @@ def expand_tree(logits_of, root_token, k, n_max, width, max_depth, token_map=Non
             expand.append(len(tokens) - 1)
         if not expand or len(tokens) >= n_max:
             break
-    return dict(tokens=tokens, parents=parents, depths=depths, cum=cum, calls=step, gaps=gaps)
+    return dict(tokens=tokens, parents=parents, depths=depths, cum=cum, calls=step, gaps=gaps,
+                bad_logits=bad_logits)
 
 
 def _path(u, tokens, parents):

@@ -4,32 +4,23 @@
 // allowed).  The split-KV partials live in a file-scope device array instead.
 //
 // In host code `g_noalloc_scratch` names a host-side stand-in, not device
-// memory: its device address is looked up once per device with
-// cudaGetSymbolAddress (that device current) and passed to the kernels.
-#include <mutex>
-
+// memory: its device address is looked up with cudaGetSymbolAddress (the
+// caller's device current) on every call and passed to the kernels.  The
+// lookup allocates nothing once this file's module is loaded; it is not
+// cached, so that a context torn down and made again (cudaDeviceReset)
+// never leaves a stale address behind.
 #include "tv_internal.cuh"
 
 namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[TV_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices] = {};
-std::mutex g_scratch_mu;
-
-// Device address of the scratch array on the current device (looked up on
-// the first call per device), or nullptr when the lookup fails.
+// Device address of the scratch array in the current context, or nullptr
+// when the lookup fails.
 void* scratch_on_current_device() {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return nullptr;
-    g_scratch_addr[dev] = ptr;
-  }
-  return g_scratch_addr[dev];
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) return nullptr;
+  return ptr;
 }
 
 }  // namespace

@@ -5,7 +5,10 @@ whole vocabulary's argmax with the same tie rule (largest value, then the
 smallest token: "ADR-037 — EAGLE-3 with dynamic tree port", phase rows E5a
 and E4b.10a).  Two all-reduces over torch.distributed (NCCL on GPUs, gloo
 on CPUs): the maximum of the values, then the minimum of the indices that
-attain it.  Plumbing only: no arithmetic of the method happens here."""
+attain it.  This cross-rank step of the argmax's tie rule (a comparison per
+row, the NaN-means-empty convention, the index offset) is computed here in
+eager torch operations around the two collectives; within a rank the argmax
+is the CUDA kernel's."""
 from __future__ import annotations
 
 import torch

@@ -67,6 +67,10 @@ def test_reference_arm_runs_on_rank_zero_only(rank):
         d = json.loads(lines[-1])
         assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
         assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+        # the same workload description as the GPU arm prints, every tree row timed
+        assert d["config"]["workload"] == "tiny-fp32-d256-p24-tree8"
+        assert d["config"]["tree_rows"] == 8 and d["config"]["paged"] is False
+        assert d["rows_timed_per_step"] == 8
 
 
 def _shard_worker(rank, port, q, logits, cuts):

@@ -154,9 +154,9 @@ def test_plus_inf_row_flags_and_skips_the_node():
     rows = all_rows(spec, spec.max_nodes + 1)
     rows[1][2, 1, 17] = float("inf")
     dx = run(spec, rows=rows)
-    ref_rows = [r.clone() for r in rows]
-    ref_rows[1][2, 1, :] = float("nan")          # the oracle's reading: that node gets no children
-    check(spec, dx, oracle_trees(spec, ref_rows), status=64)
+    refs = oracle_trees(spec, rows)              # the oracle on the kernel's own input
+    assert [t["bad_logits"] for t in refs] == [False, False, True]
+    check(spec, dx, refs, status=64)
 
 
 def test_out_of_order_step_is_refused():

@@ -76,6 +76,40 @@ def test_status_bad_tree():
     assert int(st.status[0]) & 1
 
 
+def test_bad_tree_bit_matches_the_oracle_verdict():
+    # random batches of trees, some corrupted (self, forward, out-of-range or
+    # negative parents, a root with a parent): the mask kernel's bad-tree bit
+    # must equal "some tree fails oracle.check_tree", and the ancestor words of
+    # every valid tree must still equal the oracle's
+    w = workload(wl.small_variant(5, vocab=64))
+    st = DeviceStep(w)
+    rng = np.random.default_rng(23)
+    seen = set()
+    for case in range(40):
+        trees = []
+        for b in range(w.batch):
+            par = list(w.parents[b])
+            n = len(par)
+            if rng.random() < 0.3:
+                j = int(rng.integers(0, n))
+                par[j] = int(rng.choice([-2, -1, j, min(j + 1, n), n + 5, 0]))
+            trees.append(par)
+        st.parents.copy_(torch.tensor([x for t in trees for x in t], dtype=torch.int32))
+        st.status.zero_()
+        st.mask()
+        torch.cuda.synchronize()
+        want_bad = not all(oracle.check_tree(t) for t in trees)
+        assert bool(int(st.status[0]) & 1) == want_bad, (case, trees)
+        seen.add(want_bad)
+        anc = st.anc.cpu().tolist()
+        for b, t in enumerate(trees):
+            if oracle.check_tree(t):
+                o0, _ = w.seq_rows(b)
+                for i, s in enumerate(oracle.ancestors(t)):
+                    assert (anc[o0 + i] & ((1 << 64) - 1)) == sum(1 << j for j in s)
+    assert seen == {True, False}
+
+
 def test_status_capacity_leaves_cache():
     spec = wl.CONFIGS[2].replace(prefix=(100, 100), vocab=64, cache_margin=0, p_match=1.0)
     w = workload(spec)

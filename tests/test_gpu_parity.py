@@ -83,3 +83,16 @@ def test_merge_in_batches():
     from speculative_decoding_tree_gb300 import tv_attn_plan
     assert tv_attn_plan(st.desc)["num_splits"] > 24
     check_step(w, st, oracle.verify_step(w))
+
+
+@pytest.mark.parametrize("batch,seed", [(4, 61), (6, 62)])
+def test_batched_multi_chunk_every_element(batch, seed):
+    # ragged paged batches whose prefixes span several key chunks (4096 to
+    # 8192 keys) with random 16-64-node trees: every (row, head) output is
+    # compared with the oracle, at a vocabulary small enough for the oracle
+    spec = wl.CONFIGS[5].replace(batch=batch, prefix=(4096, 8192), vocab=2053, seed=seed)
+    w = workload(spec)
+    st = run(w)
+    from speculative_decoding_tree_gb300 import tv_attn_plan
+    assert tv_attn_plan(st.desc)["num_splits"] >= 3
+    check_step(w, st, oracle.verify_step(w))

@@ -260,3 +260,56 @@ def test_commit_capacity_boundary():
     kc, vc, newp = oracle.commit(w, acc)
     assert int(newp[0]) == w.capacity - 2
     assert torch.equal(kc.view(torch.int16), w.k_cache.view(torch.int16))
+
+
+# ---------------------------------------------------------------- tree validity
+
+def test_check_tree_hand_cases():
+    # a parent array is a tree in topological order exactly when the root's
+    # parent is -1 and every other node points at an earlier node
+    assert oracle.check_tree([-1])
+    assert oracle.check_tree([-1, 0, 0, 1, 1, 2, 3, 5])          # the tiny workload's tree
+    assert oracle.check_tree([-1, 0, 1, 2, 3])                   # a chain
+    assert oracle.check_tree([-1, 0, 0, 0, 0])                   # a star
+    assert not oracle.check_tree([])                             # no root
+    assert not oracle.check_tree([0])                            # root with a parent
+    assert not oracle.check_tree([-1, -1])                       # a second root
+    assert not oracle.check_tree([-1, 1])                        # a self parent
+    assert not oracle.check_tree([-1, 0, 3, 1])                  # a forward parent
+    assert not oracle.check_tree([-1, 0, 0, -2])                 # a negative parent below -1
+    assert not oracle.check_tree([-1, 0, 7])                     # a parent past the end
+    assert not oracle.check_tree([2, -1, 0])                     # the root not first
+
+
+def test_check_tree_counts_recursive_trees():
+    # closed form: with parent[0] = -1 and parent[i] in {0 .. i-1}, node i has
+    # i choices, so exactly (n-1)! of the (n+3)^n arrays over {-2 .. n} are
+    # valid; any mistake in the bounds (<= i, >= -1, a free root) changes the count
+    import math
+    for n in range(1, 6):
+        count = sum(oracle.check_tree(list(p)) for p in itertools.product(range(-2, n + 1), repeat=n))
+        assert count == math.factorial(n - 1), n
+
+
+def test_check_tree_agrees_with_the_ancestor_walk():
+    # on random arrays, validity equals "every node's parent chain reaches the
+    # root through strictly smaller indices", checked here by a separate walk
+    rng = np.random.default_rng(11)
+    seen = {True: 0, False: 0}
+    for _ in range(400):
+        n = int(rng.integers(1, 12))
+        p = [-1] + [int(rng.integers(0, i)) for i in range(1, n)]
+        if rng.random() < 0.5:
+            j = int(rng.integers(0, n))
+            p[j] = int(rng.integers(-2, n + 1))
+        ok = True
+        for i in range(n):
+            j, steps = i, 0
+            while j != 0 and ok:
+                q = p[j]
+                ok = 0 <= q < j
+                j, steps = (q if ok else 0), steps + 1
+            ok = ok and p[0] == -1
+        assert oracle.check_tree(p) == ok
+        seen[ok] += 1
+    assert seen[True] > 50 and seen[False] > 50

@@ -225,3 +225,24 @@ def test_equal_values_go_to_the_first_generated():
     assert t["tokens"] == [3, 0, 1, 0, 1]
     assert t["parents"] == [-1, 0, 0, 1, 1]
     assert t["cum"][3] == 0.0 and np.isneginf(t["cum"][4])
+
+
+def test_plus_inf_row_gives_no_children():
+    # hand-derived: K = 2, W = 1, budget 4, vocabulary 3.  Root row [1, 0, -inf]:
+    # A = token 0 at 1 - log(e + 1), B = token 1 at -log(e + 1); step 0 moves A.
+    # Step 1 expands A with a row holding +inf: outside the log-softmax's
+    # domain, so A gets no children and the expansion reports it; B moves.
+    # Step 2 expands B with [0, 0, 0]: B.0 (token 0, first generated) enters
+    # at -log(e + 1) - log 3 and fills the budget.
+    inf = np.inf
+    table = np.array([[[1.0, 0.0, -inf]], [[0.0, inf, 0.0]], [[0.0, 0.0, 0.0]]])
+    t = expand.expand_tree(expand.table_drafter(table), 7, k=2, n_max=4, width=1, max_depth=5)
+    assert t["bad_logits"]
+    assert t["tokens"] == [7, 0, 1, 0]
+    assert t["parents"] == [-1, 0, 0, 2]
+    assert t["depths"] == [0, 1, 1, 2]
+    lse = np.log(np.e + 1.0)
+    assert np.allclose(t["cum"], [0.0, 1.0 - lse, -lse, -lse - np.log(3.0)], rtol=0, atol=1e-15)
+    # without the +inf entry nothing is reported
+    table[1, 0, 1] = 0.0
+    assert not expand.expand_tree(expand.table_drafter(table), 7, k=2, n_max=4, width=1, max_depth=5)["bad_logits"]
