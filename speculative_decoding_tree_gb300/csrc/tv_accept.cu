@@ -124,6 +124,30 @@ __device__ __forceinline__ int vec_first(const uint4& u, float x) {
   return 3;
 }
 
+// L2 prefetches a pass block issues while the previous kernel runs (a
+// prefetch does not read data before the wait, it only warms the cache):
+// its slice of the logits and, from the blocks of chunk 0, the row's tree K
+// and V (every KV head), which the commit may copy into the cache.
+template <int ES>
+__device__ __forceinline__ void prefetch_pass_t(const AcceptParams& p, int row, int v0, int v1) {
+  if (v0 < v1) {
+    const char* base = reinterpret_cast<const char*>(p.logits) + ((int64_t)row * p.V + v0) * ES;
+    const int64_t bytes = (int64_t)(v1 - v0) * ES;
+    for (int64_t off = (int64_t)threadIdx.x * 128; off < bytes; off += 128 * (int64_t)blockDim.x)
+      prefetch_l2(base + off);
+  }
+  if (blockIdx.x == 0) {
+    const int64_t row_bytes = (int64_t)p.d * p.esize;
+    const int lines = (int)(row_bytes / 128);
+    for (int e = threadIdx.x; e < 2 * p.Hkv * lines; e += blockDim.x) {
+      const int kind = e / (p.Hkv * lines), g = (e / lines) % p.Hkv, ln = e % lines;
+      const char* src = reinterpret_cast<const char*>(kind ? p.v_tree : p.k_tree);
+      prefetch_l2(src + ((int64_t)g * p.R + row) * row_bytes + ln * 128);
+    }
+  }
+}
+#define prefetch_pass(p, row, v0, v1) prefetch_pass_t<ES>(p, row, v0, v1)
+
 // grid (vchunks, R): one block reduces one vocab chunk of one row.  Each
 // thread streams 16-byte words (four in flight) in increasing index order.
 // A packed max over each batch of words is compared with the thread's best:
@@ -131,24 +155,17 @@ __device__ __forceinline__ int vec_first(const uint4& u, float x) {
 // word, then first element, holding it), so equal values keep the earlier
 // index and NaN never wins.  Scalar loads cover the ragged chunk ends.
 template <bool BF16>
-__global__ __launch_bounds__(256) void argmax_partial_kernel(const void* __restrict__ logits, int V, int vlen,
-                                                             int vchunks, float* __restrict__ am_val,
-                                                             int32_t* __restrict__ am_idx) {
+__global__ __launch_bounds__(256) void argmax_partial_kernel(const AcceptParams p) {
   constexpr int ES = BF16 ? 2 : 4;
   constexpr int PER = 16 / ES;                       // elements per 16-byte load
   constexpr int UNROLL = 4;                          // words in flight per thread
+  const void* __restrict__ logits = p.logits;
+  const int V = p.V;
   const int row = blockIdx.y, c = blockIdx.x;
-  const int v0 = c * vlen;
-  const int v1 = min(V, v0 + vlen);
+  const int v0 = c * p.vchunk_len;
+  const int v1 = min(V, v0 + p.vchunk_len);
   const int64_t rbase = (int64_t)row * V;            // element index of the row start
-  {
-    // pull this block's slice of the logits into L2 while the previous
-    // kernel runs (a prefetch does not read data before the wait)
-    const char* base = reinterpret_cast<const char*>(logits) + (rbase + v0) * ES;
-    const int64_t bytes = (int64_t)(v1 - v0) * ES;
-    for (int64_t off = (int64_t)threadIdx.x * 128; off < bytes; off += 128 * (int64_t)blockDim.x)
-      prefetch_l2(base + off);
-  }
+  prefetch_pass(p, row, v0, v1);
   dep_wait();
   dep_launch();
   const uintptr_t addr0 = reinterpret_cast<uintptr_t>(logits) + (uintptr_t)((rbase + v0) * ES);
@@ -204,8 +221,8 @@ __global__ __launch_bounds__(256) void argmax_partial_kernel(const void* __restr
   if (threadIdx.x == 0) {
     Best r = red[0];
     for (int k = 1; k < (int)(blockDim.x >> 5); ++k) r = better(r, red[k]);
-    am_val[(int64_t)row * vchunks + c] = r.v;
-    am_idx[(int64_t)row * vchunks + c] = r.i;
+    p.am_val[(int64_t)row * p.vchunks + c] = r.v;
+    p.am_idx[(int64_t)row * p.vchunks + c] = r.i;
   }
 }
 
@@ -262,22 +279,17 @@ __device__ __forceinline__ float gumbel_of(uint32_t w) {
 // reach the thread's best even with the largest possible noise is skipped
 // without drawing its noise (the skip is exact: the bound is never met).
 template <bool BF16>
-__global__ __launch_bounds__(256) void sample_partial_kernel(const void* __restrict__ logits, int V, int vlen,
-                                                            int vchunks, float inv_t, uint32_t k0, uint32_t k1,
-                                                            uint32_t off0, uint32_t off1,
-                                                            float* __restrict__ am_val,
-                                                            int32_t* __restrict__ am_idx) {
+__global__ __launch_bounds__(256) void sample_partial_kernel(const AcceptParams p) {
   constexpr int ES = BF16 ? 2 : 4;
+  const void* __restrict__ logits = p.logits;
+  const int V = p.V;
+  const float inv_t = p.inv_temp;
+  const uint32_t k0 = p.seed_lo, k1 = p.seed_hi, off0 = p.off_lo, off1 = p.off_hi;
   const int row = blockIdx.y, c = blockIdx.x;
-  const int v0 = c * vlen;                           // a multiple of 8
-  const int v1 = min(V, v0 + vlen);
+  const int v0 = c * p.vchunk_len;                   // a multiple of 8
+  const int v1 = min(V, v0 + p.vchunk_len);
   const int64_t rbase = (int64_t)row * V;
-  {
-    const char* base = reinterpret_cast<const char*>(logits) + (rbase + v0) * ES;
-    const int64_t bytes = (int64_t)(v1 - v0) * ES;
-    for (int64_t off = (int64_t)threadIdx.x * 128; off < bytes; off += 128 * (int64_t)blockDim.x)
-      prefetch_l2(base + off);
-  }
+  prefetch_pass(p, row, v0, v1);
   dep_wait();
   dep_launch();
   // four consecutive entries load as one word when the row keeps them aligned
@@ -339,57 +351,71 @@ __global__ __launch_bounds__(256) void sample_partial_kernel(const void* __restr
   if (threadIdx.x == 0) {
     Best r = red[0];
     for (int k = 1; k < (int)(blockDim.x >> 5); ++k) r = better(r, red[k]);
-    am_val[(int64_t)row * vchunks + c] = r.v;
-    am_idx[(int64_t)row * vchunks + c] = r.i;
+    p.am_val[(int64_t)row * p.vchunks + c] = r.v;
+    p.am_idx[(int64_t)row * p.vchunks + c] = r.i;
   }
 }
 
 // ----------------------------------------------------------------- A4 + A5
 
-// One block per sequence.  The block finishes the argmax of every node from
-// its chunk partials (four threads per node); warp 0 builds ancestors and
+// The walk and commit of one sequence, run by one block of 256 threads:
+// the block finishes the argmax of every node from its chunk partials (four
+// threads per node) or takes the given one; warp 0 builds ancestors and
 // depths and walks (lane i owns nodes i and i + 32; ballots and shuffles, no
 // shared atomics); then the block copies the accepted K/V rows into the
 // cache, and thread 0 advances prefix_len.
 constexpr int kCommitPages = kMaxNodes / kPageSize + 1;   // pages the k + 1 <= 64 rows can touch
-constexpr int kCommitRows = 1024;                           // rows per pass of the commit copy
+constexpr int kCommitRows = 256;                            // rows per pass of the commit copy
+constexpr int kWalkThreads = 256;
 
-__global__ __launch_bounds__(256) void walk_commit_kernel(AcceptParams p) {
-  __shared__ int s_par[kMaxNodes], s_draft[kMaxNodes], s_am[kMaxNodes], s_path[kMaxNodes];
-  __shared__ uint64_t s_anc[kMaxNodes];
-  __shared__ int s_pid[kCommitPages];
-  __shared__ const uint4* s_src[kCommitRows];
-  __shared__ uint4* s_dst[kCommitRows];
-  __shared__ int s_k, s_ok;
+struct WalkSmem {
+  int par[kMaxNodes], draft[kMaxNodes], am[kMaxNodes], path[kMaxNodes];
+  uint64_t anc[kMaxNodes];
+  int pid[kCommitPages];
+  const uint4* src[kCommitRows];
+  uint4* dst[kCommitRows];
+  int k, ok;
+};
 
-  const int b = blockIdx.x;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // The sequence's lengths, parents, drafts and pages come from before the
-  // argmax pass (which writes none of them and waited for its own
-  // predecessor before letting this kernel start), so they are read before
-  // the dependency wait; only the argmax partials wait for it.
-  int o0 = 0, n = 0;
-  const bool valid = seq_rows(p.node_offsets, b, p.R, p.max_nodes, nullptr, &o0, &n);
-  const int P = valid ? p.prefix_len[b] : 0;
-  if (valid) {
-    if (tid < n) {
-      s_par[tid] = p.parents[o0 + tid];
-      s_draft[tid] = p.draft[o0 + tid];
-    }
-    // page ids of the positions P .. P + n - 1 a commit may write
-    if (p.paged && tid >= 64 && tid < 64 + kCommitPages && P >= 0) {
-      const int64_t pg = (int64_t)P / kPageSize + (tid - 64);
-      s_pid[tid - 64] = pg < p.max_pages ? p.page_table[(int64_t)b * p.max_pages + pg] : -1;
-    }
+// what warp 0 keeps of the tree (lane i: nodes i and i + 32)
+struct WalkRegs {
+  uint64_t anc[2];
+  int dep[2];
+  bool tree_ok[2];
+};
+
+// Part 1, which needs no argmax.  walk_stage: the sequence's parents,
+// drafts and the page ids a commit may write (the positions P .. P + 63,
+// paged cache only), into shared memory.
+__device__ __forceinline__ void walk_stage_pages(const AcceptParams& p, int b, WalkSmem& s, int P) {
+  const int tid = threadIdx.x;
+  if (p.paged && tid >= 64 && tid < 64 + kCommitPages && P >= 0) {
+    const int64_t pg = (int64_t)P / kPageSize + (tid - 64);
+    s.pid[tid - 64] = pg < p.max_pages ? p.page_table[(int64_t)b * p.max_pages + pg] : -1;
   }
-  // ancestors and depth of each node by walking parents (warp 0, lane i
-  // owns nodes i and i + 32): they need no argmax, so they overlap the
-  // argmax pass too
-  uint64_t anc[2] = {0ull, 0ull};
-  int dep[2] = {0, 0};
-  bool tree_ok[2] = {true, true};
+}
+
+__device__ void walk_stage(const AcceptParams& p, int b, WalkSmem& s, int o0, int n, int P) {
+  const int tid = threadIdx.x;
+  if (tid < n) {
+    s.par[tid] = p.parents[o0 + tid];
+    s.draft[tid] = p.draft[o0 + tid];
+  }
+  walk_stage_pages(p, b, s, P);
+}
+
+// walk_tree: once the parents are staged, warp 0 builds each node's
+// ancestor word and depth by walking the parent pointers.
+__device__ void walk_tree(WalkSmem& s, WalkRegs& wr, int n) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int hlf = 0; hlf < 2; ++hlf) {
+    wr.anc[hlf] = 0ull;
+    wr.dep[hlf] = 0;
+    wr.tree_ok[hlf] = true;
+  }
   __syncthreads();                                  // parents staged
-  if (valid && warp == 0) {
+  if (warp == 0) {
 #pragma unroll
     for (int hlf = 0; hlf < 2; ++hlf) {
       const int i = lane + 32 * hlf;
@@ -399,7 +425,7 @@ __global__ __launch_bounds__(256) void walk_commit_kernel(AcceptParams p) {
         bool ok = true;
         while (true) {                              // terminates: the chain index strictly falls
           bits |= 1ull << j;
-          const int q = s_par[j];
+          const int q = s.par[j];
           if (j == 0) {
             ok = (q == -1);
             break;
@@ -415,28 +441,33 @@ __global__ __launch_bounds__(256) void walk_commit_kernel(AcceptParams p) {
           bits = 1ull << i;
           d = 0;
         }
-        anc[hlf] = bits;
-        dep[hlf] = d;
-        tree_ok[hlf] = ok;
-        s_anc[i] = bits;
+        wr.anc[hlf] = bits;
+        wr.dep[hlf] = d;
+        wr.tree_ok[hlf] = ok;
+        s.anc[i] = bits;
       }
     }
   }
-  dep_wait();
-  dep_launch();
-  if (!valid) {
-    if (tid == 0) set_status(p.status, TV_DEV_BAD_OFFSETS);
-    if (tid < p.max_nodes) {
-      p.path[(int64_t)b * p.max_nodes + tid] = -1;
-      p.tokens[(int64_t)b * p.max_nodes + tid] = -1;
-    }
-    if (tid == 0) p.accept_len[b] = -1;
-    return;
+}
+
+// The outputs of a sequence whose node offsets are invalid.
+__device__ void walk_invalid(const AcceptParams& p, int b) {
+  const int tid = threadIdx.x;
+  if (tid == 0) set_status(p.status, TV_DEV_BAD_OFFSETS);
+  if (tid < p.max_nodes) {
+    p.path[(int64_t)b * p.max_nodes + tid] = -1;
+    p.tokens[(int64_t)b * p.max_nodes + tid] = -1;
   }
+  if (tid == 0) p.accept_len[b] = -1;
+}
+
+// Part 2: each node's argmax (the caller's, or finished from the chunk
+// partials, which other blocks of the same grid may have written: read
+// through L2), the walk, the outputs, the commit and the new prefix length.
+__device__ void walk_finish(const AcceptParams& p, int b, WalkSmem& s, const WalkRegs& wr, int o0, int n, int P) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (p.given_argmax) {
-    // the caller's argmax (e.g. the fused lm_head's): written by the
-    // previous kernel, so read after the dependency wait
-    if (tid < n) s_am[tid] = p.argmax[o0 + tid];
+    if (tid < n) s.am[tid] = p.argmax[o0 + tid];
   } else {
     // argmax of node tid / 4 from chunks c = tid % 4, + 4, ...; max value,
     // smallest index (better() is order-free), NaN never enters
@@ -445,7 +476,8 @@ __global__ __launch_bounds__(256) void walk_commit_kernel(AcceptParams p) {
     Best bst{-FLT_MAX, -1};
     if (i < n)
       for (int c = tid & 3; c < vc; c += 4)
-        bst = better(bst, Best{p.am_val[(int64_t)(o0 + i) * vc + c], p.am_idx[(int64_t)(o0 + i) * vc + c]});
+        bst = better(bst, Best{__ldcg(p.am_val + (int64_t)(o0 + i) * vc + c),
+                               __ldcg(p.am_idx + (int64_t)(o0 + i) * vc + c)});
 #pragma unroll
     for (int off = 1; off < 4; off <<= 1) {
       Best o;
@@ -455,7 +487,7 @@ __global__ __launch_bounds__(256) void walk_commit_kernel(AcceptParams p) {
     }
     if (i < n && (tid & 3) == 0) {
       const int am = bst.i < 0 ? 0 : bst.i;
-      s_am[i] = am;
+      s.am[i] = am;
       p.argmax[o0 + i] = am;
     }
   }
@@ -469,8 +501,8 @@ __global__ __launch_bounds__(256) void walk_commit_kernel(AcceptParams p) {
     for (int hlf = 0; hlf < 2; ++hlf) {
       const int i = lane + 32 * hlf;
       if (i < n) {
-        bad |= !tree_ok[hlf];
-        mt[hlf] = (i == 0) || (tree_ok[hlf] && s_draft[i] == s_am[s_par[i]]);
+        bad |= !wr.tree_ok[hlf];
+        mt[hlf] = (i == 0) || (wr.tree_ok[hlf] && s.draft[i] == s.am[s.par[i]]);
       }
     }
     if (__any_sync(all, bad) && lane == 0) set_status(p.status, TV_DEV_BAD_TREE);
@@ -481,16 +513,16 @@ __global__ __launch_bounds__(256) void walk_commit_kernel(AcceptParams p) {
 #pragma unroll
     for (int hlf = 0; hlf < 2; ++hlf) {
       const int i = lane + 32 * hlf;
-      if (i < n && (anc[hlf] & ~match) == 0) key = max(key, (dep[hlf] << 8) | (255 - i));
+      if (i < n && (wr.anc[hlf] & ~match) == 0) key = max(key, (wr.dep[hlf] << 8) | (255 - i));
     }
     key = __reduce_max_sync(all, key);              // >= 0: the root is always reachable
     const int end = 255 - (key & 255), k = key >> 8;
     __syncwarp();
-    const uint64_t end_anc = s_anc[end];
+    const uint64_t end_anc = s.anc[end];
 #pragma unroll
     for (int hlf = 0; hlf < 2; ++hlf) {
       const int i = lane + 32 * hlf;
-      if (i < n && ((end_anc >> i) & 1ull)) s_path[dep[hlf]] = i;
+      if (i < n && ((end_anc >> i) & 1ull)) s.path[wr.dep[hlf]] = i;
     }
     __syncwarp();
 #pragma unroll
@@ -498,8 +530,8 @@ __global__ __launch_bounds__(256) void walk_commit_kernel(AcceptParams p) {
       const int t = lane + 32 * hlf;
       if (t < p.max_nodes) {
         const int64_t o = (int64_t)b * p.max_nodes + t;
-        p.path[o] = t <= k ? s_path[t] : -1;
-        p.tokens[o] = t < k ? s_draft[s_path[t + 1]] : (t == k ? s_am[end] : -1);
+        p.path[o] = t <= k ? s.path[t] : -1;
+        p.tokens[o] = t < k ? s.draft[s.path[t + 1]] : (t == k ? s.am[end] : -1);
       }
     }
     // can the k+1 rows be committed?
@@ -516,7 +548,7 @@ __global__ __launch_bounds__(256) void walk_commit_kernel(AcceptParams p) {
       for (int hlf = 0; hlf < 2; ++hlf) {
         const int t = lane + 32 * hlf;
         if (t <= k) {
-          const int pid = s_pid[(P + t) / kPageSize - P / kPageSize];
+          const int pid = s.pid[(P + t) / kPageSize - P / kPageSize];
           page_bad |= (pid < 0 || pid >= p.num_pages);
         }
       }
@@ -527,16 +559,16 @@ __global__ __launch_bounds__(256) void walk_commit_kernel(AcceptParams p) {
     }
     if (lane == 0) {
       p.accept_len[b] = k;
-      s_k = k;
-      s_ok = ok ? 1 : 0;
+      s.k = k;
+      s.ok = ok ? 1 : 0;
     }
   }
   __syncthreads();
-  if (!s_ok) return;
-  const int k = s_k;
+  if (!s.ok) return;
+  const int k = s.k;
   // copy k+1 rows x Hkv heads of K and of V: one thread per row writes the
   // row's source and destination into a table, then the block moves 16-byte
-  // units (unit u of the list: row u / units_row), up to 16 loads in flight
+  // units (unit u of the list: row u / units_row), up to 8 loads in flight
   // per thread, all issued before the stores
   const int64_t row_bytes = (int64_t)p.d * p.esize;
   const int units_row = (int)(row_bytes / 16);      // a power of two (16 .. 128)
@@ -550,39 +582,64 @@ __global__ __launch_bounds__(256) void walk_commit_kernel(AcceptParams p) {
       const int64_t pos = (int64_t)P + t;
       int64_t drow;
       if (p.paged) {
-        const int pid = s_pid[(P + t) / kPageSize - P / kPageSize];
+        const int pid = s.pid[(P + t) / kPageSize - P / kPageSize];
         drow = ((int64_t)pid * p.Hkv + g) * kPageSize + pos % kPageSize;
       } else {
         drow = ((int64_t)b * p.Hkv + g) * p.capacity + pos;
       }
-      s_src[r] = reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(kind ? p.v_tree : p.k_tree) +
-                                                ((int64_t)g * p.R + o0 + s_path[t]) * row_bytes);
-      s_dst[r] = reinterpret_cast<uint4*>(reinterpret_cast<char*>(kind ? p.v_cache : p.k_cache) + drow * row_bytes);
+      s.src[r] = reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(kind ? p.v_tree : p.k_tree) +
+                                                ((int64_t)g * p.R + o0 + s.path[t]) * row_bytes);
+      s.dst[r] = reinterpret_cast<uint4*>(reinterpret_cast<char*>(kind ? p.v_cache : p.k_cache) + drow * row_bytes);
     }
     __syncthreads();
-    constexpr int U = 16;
+    constexpr int U = 8;
     const int total = cn * units_row;
     for (int base = 0; base < total; base += U * (int)blockDim.x) {
       uint4 v[U];
-      uint4* dst[U];
 #pragma unroll
       for (int q = 0; q < U; ++q) {
         const int u = base + q * (int)blockDim.x + tid;
-        dst[q] = nullptr;
-        if (u < total) {
-          const int r = u >> ushift, cu = u & (units_row - 1);
-          v[q] = s_src[r][cu];
-          dst[q] = s_dst[r] + cu;
-        }
+        if (u < total) v[q] = s.src[u >> ushift][u & (units_row - 1)];
       }
 #pragma unroll
-      for (int q = 0; q < U; ++q)
-        if (dst[q]) *dst[q] = v[q];
+      for (int q = 0; q < U; ++q) {
+        const int u = base + q * (int)blockDim.x + tid;
+        if (u < total) s.dst[u >> ushift][u & (units_row - 1)] = v[q];
+      }
     }
     __syncthreads();
   }
-  __syncthreads();
   if (tid == 0) p.prefix_len[b] = P + k + 1;
+}
+
+// Walk and commit, one block per sequence.  After the pass kernel of the
+// same call (which writes only the chunk partials and waited for its own
+// predecessor before letting this kernel start), the sequence's lengths,
+// parents, drafts and page ids are read and the ancestors built before the
+// dependency wait; on a given argmax (no pass kernel), everything it reads
+// may come from the kernel just before it, so it waits first.
+__global__ __launch_bounds__(kWalkThreads) void walk_commit_kernel(AcceptParams p) {
+  __shared__ WalkSmem s;
+  if (p.given_argmax) {
+    dep_wait();
+    dep_launch();
+  }
+  const int b = blockIdx.x;
+  int o0 = 0, n = 0;
+  const bool valid = seq_rows(p.node_offsets, b, p.R, p.max_nodes, nullptr, &o0, &n);
+  const int P = valid ? p.prefix_len[b] : 0;
+  if (valid) walk_stage(p, b, s, o0, n, P);
+  WalkRegs wr;
+  walk_tree(s, wr, valid ? n : 0);
+  if (!p.given_argmax) {
+    dep_wait();
+    dep_launch();
+  }
+  if (!valid) {
+    walk_invalid(p, b);
+    return;
+  }
+  walk_finish(p, b, s, wr, o0, n, P);
 }
 
 }  // namespace
@@ -594,18 +651,14 @@ cudaError_t launch_tree_mask(const int32_t* parents, const int32_t* offs, uint64
 }
 
 cudaError_t launch_accept_commit(const AcceptParams& p, cudaStream_t s) {
-  if (p.given_argmax) return launch_dep(walk_commit_kernel, dim3(p.B), dim3(256), 0, s, p);
-  dim3 grid(p.vchunks, p.R);
-  cudaError_t e;
-  if (p.sampled)
-    e = launch_dep(p.logits_bf16 ? sample_partial_kernel<true> : sample_partial_kernel<false>, grid, dim3(256), 0, s,
-                   p.logits, p.V, p.vchunk_len, p.vchunks, p.inv_temp, p.seed_lo, p.seed_hi, p.off_lo, p.off_hi,
-                   p.am_val, p.am_idx);
-  else
-    e = launch_dep(p.logits_bf16 ? argmax_partial_kernel<true> : argmax_partial_kernel<false>, grid, dim3(256), 0, s,
-                   p.logits, p.V, p.vchunk_len, p.vchunks, p.am_val, p.am_idx);
-  if (e != cudaSuccess) return e;
-  return launch_dep(walk_commit_kernel, dim3(p.B), dim3(256), 0, s, p);
+  if (!p.given_argmax) {
+    dim3 grid(p.vchunks, p.R);
+    cudaError_t e = launch_dep(p.sampled ? (p.logits_bf16 ? sample_partial_kernel<true> : sample_partial_kernel<false>)
+                                         : (p.logits_bf16 ? argmax_partial_kernel<true> : argmax_partial_kernel<false>),
+                               grid, dim3(256), 0, s, p);
+    if (e != cudaSuccess) return e;
+  }
+  return launch_dep(walk_commit_kernel, dim3(p.B), dim3(kWalkThreads), 0, s, p);
 }
 
 }  // namespace tv

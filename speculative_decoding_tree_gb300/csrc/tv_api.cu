@@ -176,6 +176,8 @@ void accept_chunks(int R, int V, int* vchunks, int* vchunk_len) {
   *vchunks = (int)((V + len - 1) / len);
 }
 
+// Accept area of the workspace: the chunk partials (value and index per row
+// and vocabulary chunk).
 int64_t accept_bytes(const tv_desc* d, int V) {
   if (V <= 0) return 0;
   int vc, vl;
