@@ -521,7 +521,8 @@ def attn_summary(tv, h, bd, peak, peak_kind):
     plan = tv.tv_attn_plan(h.sets[0].desc)
     achieved = ab["split"] / (bd["split"] * 1e-6) / 1e9
     roof = {
-        "kernel": {0: "attn_simt_kernel", 1: "tv_attn_tc_kernel", 2: "tv_attn_tc2_kernel"}[plan["kernel"]],
+        "kernel": {0: "attn_simt_kernel", 1: "tv_attn_tc_kernel", 2: "tv_attn_tc2_kernel",
+                   3: "tv_attn_tcp_kernel"}[plan["kernel"]],
         "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
         "frac": round(achieved / peak, 4), "peak_source": peak_kind,
         "traffic": profiled_traffic(h.spec.name),

@@ -78,6 +78,8 @@ struct Plan {
   int tree_tile;             // num_chunks rule: 0, or the key tile (one-wave plans)
   int tile_stride;
   int64_t o_part_bytes, ml_part_bytes;
+  int64_t counter_bytes;     // the persistent kernel's work counter (0 for the other kernels)
+  int64_t part_bytes() const { return o_part_bytes + ml_part_bytes + counter_bytes; }
 };
 
 int make_plan(const tv_desc* d, Plan* p) {
@@ -98,6 +100,9 @@ int make_plan(const tv_desc* d, Plan* p) {
   // tile is faster there even though the larger trees read their K/V twice
   // (the batched workload: 137 against 159 us)
   const bool pairs = tc && row_tiles >= 2 && d->batch == 1;
+  // a batch on head_dim 128 with a bf16 output: one persistent CTA per SM
+  // takes (sequence, KV head, row tile, chunk) units from a work counter
+  const bool persist = tc && d->batch > 1 && d->head_dim == 128 && !d->out_f32;
   const int launched_tiles = pairs ? 2 * ((row_tiles + 1) / 2) : row_tiles;
   int64_t units = (int64_t)d->batch * d->num_kv_heads * launched_tiles;
   int64_t sms = num_sms();
@@ -131,16 +136,19 @@ int make_plan(const tv_desc* d, Plan* p) {
   // launch grids put sequences on z and (KV head, split) or (KV head, row
   // tile) on y, whose limit is 65535: refused here rather than at launch
   const int64_t grid_y = tc ? (int64_t)d->num_kv_heads * splits : (int64_t)splits;
-  if (d->batch > kMaxGridYZ || grid_y > kMaxGridYZ || (int64_t)d->num_kv_heads * row_tiles > kMaxGridYZ)
-    return TV_ERR_SHAPE;
+  if (d->batch > kMaxGridYZ || (int64_t)d->num_kv_heads * row_tiles > kMaxGridYZ) return TV_ERR_SHAPE;
+  // the persistent kernel's work counter counts in 24 bits; the others put
+  // (KV head, split) on grid y
+  if (persist ? grid + sms >= ((int64_t)1 << 24) : grid_y > kMaxGridYZ) return TV_ERR_SHAPE;
   p->G = G;
   p->tree_tile = tree_tile;
-  p->pub.kernel = pairs ? 2 : (tc ? 1 : 0);
+  p->pub.kernel = persist ? 3 : (pairs ? 2 : (tc ? 1 : 0));
   p->pub.num_splits = splits;
   p->pub.chunk = (int)chunk;
   p->pub.row_tiles = row_tiles;
   p->pub.rows_per_tile = rows_per_tile;
-  p->pub.grid_ctas = (int)grid;
+  p->pub.grid_ctas = (int)(persist ? (grid < sms ? grid : sms) : grid);
+  p->counter_bytes = persist ? 256 : 0;
   // partials are tile-major: every (split, sequence, KV head, row tile) owns
   // tile_stride rows (128 for the tensor-core kernel, whose epilogue stores
   // whole 128-row tiles)
@@ -218,6 +226,10 @@ AttnParams attn_params(const tv_desc* d, const Plan& pl, const void* q, const vo
   a.out = nullptr;
   a.out_bf16 = (d->dtype == TV_BF16 && !d->out_f32) ? 1 : 0;
   a.status = st;
+  a.work_counter = pl.counter_bytes
+                       ? reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(ws) + pl.o_part_bytes +
+                                                               pl.ml_part_bytes)
+                       : nullptr;
   a.B = d->batch; a.Hq = d->num_q_heads; a.Hkv = d->num_kv_heads; a.G = pl.G; a.d = d->head_dim;
   a.R = d->total_rows; a.max_nodes = d->max_nodes;
   a.paged = d->page_size != 0;
@@ -234,7 +246,8 @@ AttnParams attn_params(const tv_desc* d, const Plan& pl, const void* q, const vo
 }
 
 int launch_partials(const tv_desc* d, const Plan& pl, const AttnParams& a, cudaStream_t s) {
-  cudaError_t e = pl.pub.kernel == 2   ? launch_attn_tc2(a, s)
+  cudaError_t e = pl.pub.kernel == 3   ? launch_attn_tcp(a, s)
+                  : pl.pub.kernel == 2 ? launch_attn_tc2(a, s)
                   : pl.pub.kernel == 1 ? launch_attn_tc(a, s)
                                        : launch_attn_simt(a, d->dtype, s);
   return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
@@ -289,7 +302,7 @@ int accept_commit_impl(const tv_desc* desc, int32_t vocab, int32_t logits_dtype,
   Plan p;
   rc = make_plan(desc, &p);
   if (rc) return rc;
-  int64_t off = p.o_part_bytes + p.ml_part_bytes;
+  int64_t off = p.part_bytes();
   if ((int64_t)workspace_bytes < off + accept_bytes(desc, vocab)) return TV_ERR_WORKSPACE;
   AcceptParams a;
   a.given_argmax = 0;
@@ -372,7 +385,7 @@ int tv_workspace_size(const tv_desc* desc, int32_t vocab, size_t* bytes) {
   rc = make_plan(desc, &p);
   if (rc) return rc;
   int64_t total = 0;
-  if (!add_ok(p.o_part_bytes, p.ml_part_bytes, &total) || !add_ok(total, accept_bytes(desc, vocab), &total))
+  if (!add_ok(p.part_bytes(), accept_bytes(desc, vocab), &total))
     return TV_ERR_OVERFLOW;
   *bytes = (size_t)total;
   return TV_OK;
@@ -403,7 +416,7 @@ int tv_attn_partials(const tv_desc* desc, const void* d_q, const void* d_k_cache
   Plan p;
   rc = make_plan(desc, &p);
   if (rc) return rc;
-  if ((int64_t)workspace_bytes < p.o_part_bytes + p.ml_part_bytes) return TV_ERR_WORKSPACE;
+  if ((int64_t)workspace_bytes < p.part_bytes()) return TV_ERR_WORKSPACE;
   AttnParams a = attn_params(desc, p, d_q, d_k_cache, d_v_cache, d_page_table, d_prefix_len, d_node_offsets,
                              d_k_tree, d_v_tree, d_anc, d_workspace, d_status);
   return launch_partials(desc, p, a, as_stream(stream));
@@ -420,7 +433,7 @@ int tv_attn_merge(const tv_desc* desc, const int32_t* d_prefix_len, const int32_
   Plan p;
   rc = make_plan(desc, &p);
   if (rc) return rc;
-  if ((int64_t)workspace_bytes < p.o_part_bytes + p.ml_part_bytes) return TV_ERR_WORKSPACE;
+  if ((int64_t)workspace_bytes < p.part_bytes()) return TV_ERR_WORKSPACE;
   return launch_merge_from(desc, p, d_prefix_len, d_node_offsets, d_out, d_workspace, d_status,
                            as_stream(stream), 0);
 }
@@ -439,7 +452,7 @@ int tree_verify_attn(const tv_desc* desc, const void* d_q, const void* d_k_cache
   Plan p;
   rc = make_plan(desc, &p);
   if (rc) return rc;
-  if ((int64_t)workspace_bytes < p.o_part_bytes + p.ml_part_bytes) return TV_ERR_WORKSPACE;
+  if ((int64_t)workspace_bytes < p.part_bytes()) return TV_ERR_WORKSPACE;
   AttnParams a = attn_params(desc, p, d_q, d_k_cache, d_v_cache, d_page_table, d_prefix_len, d_node_offsets,
                              d_k_tree, d_v_tree, d_anc, d_workspace, d_status);
   a.out = d_out;                      // one-chunk sequences are finished by the split pass

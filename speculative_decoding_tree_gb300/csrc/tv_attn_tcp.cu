@@ -1,0 +1,725 @@
+// tcgen05 split-KV tree-verify attention for batches of sequences (bf16
+// Q/K/V, head_dim 128, bf16 output): one persistent CTA per SM.
+//
+// The arithmetic is the one-CTA kernel's (flash-decode with a tree mask,
+// "ADR-037 — EAGLE-3 with dynamic tree port", phase rows E1.1-E1.5 and
+// E4b.6, the dk128 retrofit): a work unit is (sequence b, KV head g, query
+// row tile rt, key chunk s); its keys are the chunk's prefix positions in
+// 128-key tiles and, in the sequence's last chunk, one tile of tree keys
+// masked by each row's ancestor bits; the unit leaves a normalised partial
+// O_s / l_s (bf16) with its running maximum and sum for the merge, or the
+// final rows when the sequence has one chunk.
+//
+// In a batch the sequences have different prefix lengths and tree sizes, so
+// a grid of one CTA per unit runs in uneven waves and pays the CTA's setup
+// (barriers, tensor memory, the first tiles' latency, the epilogue's drain)
+// once per unit.  Here each CTA sets up once and takes units from a work
+// counter in the workspace until none is left; units are numbered
+// chunk-major (every sequence's first chunk first), so the long full chunks
+// go out before the short last ones.  Units with no rows or no keys are
+// skipped without being handed out.
+//
+//   warp 0      TMA producer: per unit its Q tile, then 32 KB K/V chunks
+//               through a ring of slots in MMA order K(0), K(1), V(0), ...
+//               (sixteen 16-row boxes per chunk on a paged cache).
+//   warp 1      owns tensor memory; lane 0 issues the MMAs: S(t) = Q K(t)^T
+//               into one of two 128-column buffers, O += P V into one of two
+//               O buffers (alternating by unit, so that a unit's epilogue
+//               can read its O while the next unit accumulates).
+//   warp 2      scheduler (lane 0): takes unit numbers from the counter,
+//               decodes them (lengths, offsets, chunk bounds) and hands them
+//               through a two-entry queue in shared memory to the others.
+//   warps 3-10  softmax (two threads per query row, each half of a tile's
+//               keys), then each unit's epilogue, which writes the partial
+//               rows straight from registers.
+// Barrier phases run on across units: slots by a slot counter, the S / P /
+// O buffers by a tile counter, the max / sum exchanges by an exchange
+// counter, per-unit barriers by a unit counter.  Every wait is bounded
+// (1 s); on a timeout the CTA raises TV_DEV_TIMEOUT and every role leaves
+// its loop.
+//
+// The work counter needs no zeroing: its word holds a tag (the low 40 bits
+// of the launch's %gridid) above a 24-bit count.  Every CTA first raises the
+// word to (tag, 0) with an atomic maximum (an earlier launch's word has a
+// smaller tag; memory never written by a launch, with a larger one, is
+// replaced by compare-and-swap) and only then takes numbers with atomic adds.
+#include <cuda.h>
+
+#include <climits>
+#include <mutex>
+
+#include "tc_ptx.cuh"
+#include "tv_internal.cuh"
+
+namespace tv {
+namespace {
+
+using namespace tc;
+
+constexpr int D = 128;
+constexpr int BM = 128;                         // query rows per tile
+constexpr int BN = 128;                         // keys per tile
+constexpr uint32_t BOX_BYTES = BN * 128;        // one TMA box: 128 rows x 64 bf16
+constexpr uint32_t SLOT_BYTES = 2 * BOX_BYTES;  // 128 keys x 128 columns
+constexpr int NS = 6;                           // ring slots
+constexpr uint32_t kHeader = 3072;              // barriers, TMEM address, exchanges, unit queue
+constexpr uint32_t Q_BYTES = BM * D * 2;
+constexpr uint32_t SMEM = kHeader + Q_BYTES + NS * SLOT_BYTES;
+static_assert(SMEM <= 232448, "shared memory over the 227 KB per-block limit");
+constexpr int kThreads = 352;
+constexpr int kFirstSoftmaxWarp = 3;
+constexpr int kSoftmaxWarps = 8;
+constexpr uint64_t kWaitNs = 1000000000ull;
+constexpr float kRescaleThreshold = 8.0f;       // rescale O when the max grows by > 2^8
+constexpr int kUnitSlots = 2;                   // the unit queue
+constexpr int kUnitReaders = 2 + kSoftmaxWarps; // producer, MMA lane, softmax warps
+
+// barrier numbers
+constexpr int B_FULL = 0, B_EMPTY = NS, B_QFULL = 2 * NS, B_QEMPTY = B_QFULL + 1, B_SFULL = B_QEMPTY + 1,
+              B_PFULL = B_SFULL + 2, B_ODONE = B_PFULL + 2, B_XCH = B_ODONE + 2, B_TAIL = B_XCH + 2,
+              B_FIN = B_TAIL + 1, B_UFULL = B_FIN + 1, B_UEMPTY = B_UFULL + kUnitSlots,
+              NBARS = B_UEMPTY + kUnitSlots;
+static_assert(NBARS * 8 + 8 <= 256, "barriers overflow the header");
+
+struct UnitInfo {
+  int32_t valid;           // 0: no more units
+  int32_t b, g, rt, s;
+  int32_t o0, n, nch;      // the sequence's first row, node count, chunk count
+  int32_t npt, T, tail_valid, pad;
+  int64_t k_begin, k_end;  // the chunk's prefix keys
+};
+static_assert(sizeof(UnitInfo) == 64, "unit queue entry");
+constexpr uint32_t kXchOfs = 256;               // [2 parity][2 half][128 rows] floats
+constexpr uint32_t kQueueOfs = kXchOfs + 2048;
+static_assert(kQueueOfs + kUnitSlots * sizeof(UnitInfo) <= kHeader, "unit queue overflows the header");
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ unsigned long long launch_tag() {
+  unsigned long long g;
+  asm volatile("mov.u64 %0, %%gridid;" : "=l"(g));
+  return (g & ((1ull << 40) - 1)) << 24;
+}
+
+__device__ __forceinline__ void arm_counter(unsigned long long* cnt, unsigned long long tag) {
+  unsigned long long old = atomicMax(cnt, tag);
+  while ((old >> 24) > (tag >> 24)) {               // not an earlier launch's word: replace it
+    const unsigned long long prev = atomicCAS(cnt, old, tag);
+    if (prev == old) break;
+    old = prev;                                     // changed meanwhile (another CTA may have armed it)
+  }
+}
+
+// Unit u (chunk-major numbering) with everything the roles need; false when
+// it has no rows (tile past the tree's rows, invalid offsets) or no keys
+// (chunk past the sequence's prefix).
+// (Unit numbers stay below 2^24, which the host checks, so 32-bit
+// arithmetic decodes them.)
+__device__ bool decode_unit(const AttnParams& p, int u, UnitInfo& ui) {
+  const int per_s = p.B * p.Hkv * p.row_tiles;
+  const int s = u / per_s;
+  const int rem = u - s * per_s;
+  const int b = rem / (p.Hkv * p.row_tiles);
+  const int g = (rem / p.row_tiles) % p.Hkv;
+  const int rt = rem % p.row_tiles;
+  int o0 = 0, n = 1;
+  if (!seq_rows(p.node_offsets, b, p.R, p.max_nodes, p.status, &o0, &n)) return false;
+  if (rt * p.rows_per_tile >= n * p.G) return false;
+  const int64_t Praw = p.prefix_len[b];
+  const int64_t P = clamp_prefix(Praw, p.max_prefix, p.capacity);
+  if (P != Praw && rt == 0 && s == 0 && g == 0) set_status(p.status, TV_DEV_BAD_PREFIX);
+  const int nch = num_chunks(P, p.chunk, p.tree_tile);
+  if (s >= nch) return false;
+  ui.valid = 1;
+  ui.b = b;
+  ui.g = g;
+  ui.rt = rt;
+  ui.s = s;
+  ui.o0 = o0;
+  ui.n = n;
+  ui.nch = nch;
+  ui.k_begin = (int64_t)s * p.chunk;
+  ui.k_end = min(P, ui.k_begin + p.chunk);
+  ui.npt = (int)((ui.k_end - ui.k_begin + BN - 1) / BN);
+  ui.T = ui.npt + (s == nch - 1 ? 1 : 0);
+  ui.tail_valid = ui.npt > 0 ? (int)(ui.k_end - (ui.k_begin + (int64_t)(ui.npt - 1) * BN)) : BN;
+  ui.pad = 0;
+  return true;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tm_q,
+                   const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_vc,
+                   const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_vt) {
+  constexpr unsigned kAll = 0xffffffffu;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+
+  // ---------------------------------------------------------------- smem
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + NBARS * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* xch = reinterpret_cast<float*>(smem_raw + kXchOfs);
+  UnitInfo* uqueue = reinterpret_cast<UnitInfo*>(smem_raw + kQueueOfs);
+  uint8_t* sQ = smem_raw + kHeader;
+  uint8_t* ring = sQ + Q_BYTES;
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  auto FULL = [&](int i) { return bar(B_FULL + i); };
+  auto EMPTY = [&](int i) { return bar(B_EMPTY + i); };
+  const uint32_t Q_FULL = bar(B_QFULL), Q_EMPTY = bar(B_QEMPTY), TAIL = bar(B_TAIL), FIN = bar(B_FIN);
+  auto S_FULL = [&](int i) { return bar(B_SFULL + i); };
+  auto P_FULL = [&](int i) { return bar(B_PFULL + i); };
+  auto O_DONE = [&](int i) { return bar(B_ODONE + i); };
+  auto XCH = [&](int i) { return bar(B_XCH + i); };
+  auto UFULL = [&](int i) { return bar(B_UFULL + i); };
+  auto UEMPTY = [&](int i) { return bar(B_UEMPTY + i); };
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (smem_u32(smem_raw) & 1023u) {                 // the layout needs a 1 KB aligned window
+    dep_wait();
+    if (tid == 0) set_status(p.status, TV_DEV_TIMEOUT);
+    return;
+  }
+  // on-chip setup before the dependency wait (overlaps the previous kernel's tail)
+  if (tid == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(FULL(i), 1);
+      mbar_init(EMPTY(i), 1);
+    }
+    mbar_init(Q_FULL, 1);
+    mbar_init(Q_EMPTY, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(S_FULL(i), 1);
+      mbar_init(P_FULL(i), kSoftmaxWarps);
+      mbar_init(O_DONE(i), 1);
+      mbar_init(XCH(i), kSoftmaxWarps);
+    }
+    mbar_init(TAIL, 1);
+    mbar_init(FIN, 1);
+    for (int i = 0; i < kUnitSlots; ++i) {
+      mbar_init(UFULL(i), 1);
+      mbar_init(UEMPTY(i), kUnitReaders);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (p.rows_per_tile < BM) {
+    // pad rows of the query tile (G does not divide 128) hold zeros; the Q
+    // loads never write them
+    const int pad = BM - p.rows_per_tile;
+    for (int e = tid; e < (D / 64) * pad * 8; e += blockDim.x) {
+      const int kb = e / (pad * 8), r = p.rows_per_tile + (e / 8) % pad, c = e % 8;
+      *reinterpret_cast<uint4*>(sQ + kb * (BM * 128) + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_kc);
+    tma_prefetch_desc(&tm_vc);
+    tma_prefetch_desc(&tm_kt);
+    tma_prefetch_desc(&tm_vt);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  dep_wait();
+  dep_launch();
+
+  const int G = p.G;
+  if (warp == 2 && lane == 0) {
+    // ============================================================ scheduler
+    {
+      const int U = p.splits * p.B * p.Hkv * p.row_tiles;
+      const unsigned long long tag = launch_tag();
+      arm_counter(p.work_counter, tag);
+      auto next = [&]() -> int {
+        return (int)gridDim.x + (int)(atomicAdd(p.work_counter, 1ull) & 0xFFFFFFull);
+      };
+      int u = blockIdx.x;
+      int k = 0, pushes = 0;
+      while (true) {
+        UnitInfo ui;
+        ui.valid = 0;
+        while (u < U && !decode_unit(p, u, ui)) u = next();
+        if (pushes >= kUnitSlots &&
+            !mbar_wait(UEMPTY(k), ((pushes / kUnitSlots) - 1) & 1, abort_flag, kWaitNs))
+          break;                                    // aborted: every role leaves on the flag
+        volatile UnitInfo* qe = reinterpret_cast<volatile UnitInfo*>(uqueue + k);
+        qe->valid = ui.valid;
+        qe->b = ui.b;
+        qe->g = ui.g;
+        qe->rt = ui.rt;
+        qe->s = ui.s;
+        qe->o0 = ui.o0;
+        qe->n = ui.n;
+        qe->nch = ui.nch;
+        qe->npt = ui.npt;
+        qe->T = ui.T;
+        qe->tail_valid = ui.tail_valid;
+        qe->k_begin = ui.k_begin;
+        qe->k_end = ui.k_end;
+        mbar_arrive(UFULL(k));
+        ++pushes;
+        k ^= 1;
+        if (!ui.valid) break;
+        u = next();
+      }
+    }
+  } else if (warp == 0) {
+    // ============================================================ producer
+    int j = 0, tail_uses = 0, uq = 0, k = 0;
+    bool ok = true;
+    const int oob_row = p.paged ? (int)(p.num_pages * p.Hkv * kPageSize) : 0;
+    while (ok) {
+      if (!__all_sync(kAll, mbar_wait(UFULL(k), (uq / kUnitSlots) & 1, abort_flag, kWaitNs))) break;
+      const volatile UnitInfo* qe = reinterpret_cast<const volatile UnitInfo*>(uqueue + k);
+      if (!qe->valid) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(UEMPTY(k));
+        break;
+      }
+      const int b = qe->b, g = qe->g, npt = qe->npt, T = qe->T, tail_valid = qe->tail_valid, o0 = qe->o0;
+      const int q_node = o0 + qe->rt * p.rows_per_tile / G;   // the Q tile's first node
+      const int64_t k_begin = qe->k_begin, k_end = qe->k_end;
+      // The unit's Q tile replaces the previous unit's once that unit's QK
+      // products are done (Q_EMPTY).  It is loaded just before the unit's
+      // first V chunk: its first K chunks go into the ring before, so they
+      // stream in while the previous unit finishes.
+      bool q_loaded = false;
+      auto load_q = [&]() -> bool {
+        if (uq > 0 && !__all_sync(kAll, mbar_wait(Q_EMPTY, (uq - 1) & 1, abort_flag, kWaitNs))) return false;
+        if (lane == 0) {
+          mbar_expect_tx(Q_FULL, (uint32_t)p.rows_per_tile * 128u * (D / 64));
+          for (int kb = 0; kb < D / 64; ++kb)
+            tma_load_3d(smem_u32(sQ + kb * (BM * 128)), &tm_q, Q_FULL, kb * 64, g * G, q_node);
+        }
+        q_loaded = true;
+        return true;
+      };
+      auto page_id = [&](int tile) -> int {         // raw page id of this lane's page, or INT_MIN (none)
+        if (!p.paged || tile >= npt || lane >= BN / kPageSize) return INT_MIN;
+        const int64_t pos = k_begin + (int64_t)tile * BN + lane * kPageSize;
+        if (pos >= k_end) return INT_MIN;
+        return p.page_table[(int64_t)b * p.max_pages + pos / kPageSize];
+      };
+      auto page_row = [&](int pid) -> int {         // TMA row of a page id, checked where it is used
+        if (pid == INT_MIN) return -1;
+        if (pid >= 0 && pid < p.num_pages) return (int)(((int64_t)pid * p.Hkv + g) * kPageSize);
+        set_status(p.status, TV_DEV_BAD_PAGE);
+        return oob_row;                             // out of range: the copy reads zeros
+      };
+      int pid_a = page_id(0), pid_b = page_id(1), pid_c = page_id(2), pid_d = page_id(3);
+      int row_k = -1, row_v = -1;
+      for (int t = 0; t <= T && ok; ++t) {
+        row_v = row_k;
+        row_k = page_row(pid_a);
+        pid_a = pid_b;
+        pid_b = pid_c;
+        pid_c = pid_d;
+        pid_d = page_id(t + 4);
+        for (int kind = 0; kind < 2 && ok; ++kind) {         // 0: K(t), 1: V(t-1)
+          const int tile = kind == 0 ? t : t - 1;
+          if ((kind == 0 && t >= T) || (kind == 1 && t < 1)) continue;
+          if (kind == 1 && !q_loaded && !load_q()) {
+            ok = false;
+            break;
+          }
+          const bool tree = (tile == npt);
+          const bool tail_fix = (kind == 1) && !tree && tile == npt - 1 && tail_valid < BN;
+          const int slot = j % NS, use = j / NS;
+          if (use > 0 && !__all_sync(kAll, mbar_wait(EMPTY(slot), (use - 1) & 1, abort_flag, kWaitNs))) {
+            ok = false;
+            break;
+          }
+          uint8_t* dst = ring + slot * SLOT_BYTES;
+          const uint32_t fb = tail_fix ? TAIL : FULL(slot);
+          if (tree || !p.paged) {
+            if (lane == 0) {
+              mbar_expect_tx(fb, SLOT_BYTES);
+              const CUtensorMap* m = tree ? (kind == 0 ? &tm_kt : &tm_vt) : (kind == 0 ? &tm_kc : &tm_vc);
+              const int64_t row = tree ? (int64_t)g * p.R + o0
+                                       : ((int64_t)b * p.Hkv + g) * p.capacity + k_begin + (int64_t)tile * BN;
+              for (int bx = 0; bx < 2; ++bx) tma_load_2d(smem_u32(dst + bx * BOX_BYTES), m, fb, bx * 64, (int)row);
+            }
+          } else {
+            const CUtensorMap* m = kind == 0 ? &tm_kc : &tm_vc;
+            const int my_row = kind == 0 ? row_k : row_v;
+            const int npages = __popc(__ballot_sync(kAll, my_row >= 0));
+            if (lane == 0) mbar_expect_tx(fb, (uint32_t)npages * 2u * (kPageSize * 128u));
+            __syncwarp();
+            if (my_row >= 0)
+              for (int bx = 0; bx < 2; ++bx)
+                tma_load_2d(smem_u32(dst + bx * BOX_BYTES + lane * kPageSize * 128), m, fb, bx * 64, my_row);
+          }
+          __syncwarp();
+          if (tail_fix) {
+            // the chunk's rows past the prefix end become zeros before the MMA reads them
+            if (!__all_sync(kAll, mbar_wait(TAIL, tail_uses & 1, abort_flag, kWaitNs))) {
+              ok = false;
+              break;
+            }
+            ++tail_uses;
+            const int nz = BN - tail_valid;
+            for (int e = lane; e < 2 * nz * 8; e += 32) {
+              const int bx = e / (nz * 8), r = tail_valid + (e / 8) % nz, q16 = e % 8;
+              *reinterpret_cast<uint4*>(dst + bx * BOX_BYTES + r * 128 + q16 * 16) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(FULL(slot));
+          }
+          ++j;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(UEMPTY(k));       // done with the queue entry
+      k ^= 1;
+      ++uq;
+    }
+    // drain: every copy this warp started has landed before the CTA exits
+    if (lane == 0) {
+      if (uq > 0) mbar_wait(Q_FULL, (uq - 1) & 1, abort_flag, kWaitNs);
+      for (int jj = (j > NS ? j - NS : 0); jj < j; ++jj) mbar_wait(FULL(jj % NS), (jj / NS) & 1, abort_flag, kWaitNs);
+    }
+  } else if (warp == 1) {
+    // ============================================================ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t ID_QK = idesc_bf16_f32(BM, BN, 0, 0);
+      constexpr uint32_t ID_PV = idesc_bf16_f32(BM, D, 0, 1);
+      const uint32_t q_addr = smem_u32(sQ);
+      const uint32_t ring_addr = smem_u32(ring);
+      int j = 0, tt = 0, uq = 0, k = 0;
+      bool ok = true;
+      while (ok) {
+        if (!mbar_wait(UFULL(k), (uq / kUnitSlots) & 1, abort_flag, kWaitNs)) break;
+        const int T = reinterpret_cast<const volatile UnitInfo*>(uqueue + k)->valid
+                          ? reinterpret_cast<const volatile UnitInfo*>(uqueue + k)->T
+                          : 0;
+        mbar_arrive(UEMPTY(k));                     // only T is needed, and it is read
+        k ^= 1;
+        if (T == 0) break;
+        const uint32_t obuf = tmem + 256 + (uint32_t)((uq & 1) * D);
+        if (!mbar_wait(Q_FULL, uq & 1, abort_flag, kWaitNs)) break;
+        tc_fence_after();
+        for (int t = 0; t <= T && ok; ++t) {
+          if (t < T) {
+            const int tg = tt + t;
+            const uint32_t sbuf = tmem + (uint32_t)((tg & 1) * 128);
+            const int slot = j % NS;
+            if (!mbar_wait(FULL(slot), (j / NS) & 1, abort_flag, kWaitNs)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t kaddr = ring_addr + slot * SLOT_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {   // 16-column steps over d
+              const uint64_t a = smem_desc(q_addr + (kk >> 2) * (BM * 128) + (kk & 3) * 32, 16, 1024, 2);
+              const uint64_t bd = smem_desc(kaddr + (kk >> 2) * BOX_BYTES + (kk & 3) * 32, 16, 1024, 2);
+              mma_ss(sbuf, a, bd, ID_QK, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(EMPTY(slot));
+            mma_commit(S_FULL(tg & 1));
+            if (t == T - 1) mma_commit(Q_EMPTY);    // the unit's last product that reads Q
+            ++j;
+          }
+          if (t >= 1) {
+            const int u = t - 1, ug = tt + u;
+            const uint32_t pbuf = tmem + (uint32_t)((ug & 1) * 128);
+            if (!mbar_wait(P_FULL(ug & 1), (ug >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
+            tc_fence_after();
+            const int slot = j % NS;
+            if (!mbar_wait(FULL(slot), (j / NS) & 1, abort_flag, kWaitNs)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t vaddr = ring_addr + slot * SLOT_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk) {  // 16 keys per step
+              const uint64_t bd = smem_desc(vaddr + kk * (16 * 128), BOX_BYTES, 1024, 2);
+              mma_ts(obuf, pbuf + kk * 8, bd, ID_PV, (u > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(EMPTY(slot));
+            mma_commit(O_DONE(ug & 1));
+            ++j;
+          }
+        }
+        tt += T;
+        ++uq;
+      }
+      // every MMA this thread issued has finished before tensor memory is freed
+      mma_commit(FIN);
+      mbar_wait(FIN, 0, abort_flag, kWaitNs);
+    }
+  } else if (warp >= kFirstSoftmaxWarp) {
+    // ============================================================ softmax
+    // Two warpgroups: `half` 0 takes keys 0-63 of every tile (and O columns
+    // 0-63), half 1 keys 64-127 (and columns 64-127); the two threads of a
+    // row share its running maximum (and at the end its sum) through `xch`.
+    const int half = (warp - kFirstSoftmaxWarp) >> 2;
+    const int r = (warp & 3) * 32 + lane;           // row in the tile == TMEM lane (warp % 4 picks the quarter)
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const float c2 = p.scale_log2;
+    const int kofs = half * (BN / 2);
+    int tt = 0, xt = 0, uq = 0, k = 0;
+    bool ok = true;
+    while (ok) {
+      if (!__all_sync(kAll, mbar_wait(UFULL(k), (uq / kUnitSlots) & 1, abort_flag, kWaitNs))) break;
+      // the entry stays valid until this warp arrives on UEMPTY at the end of
+      // the unit: fields the epilogue needs are read there again (fewer live
+      // registers through the tile loop)
+      const volatile UnitInfo* qe = reinterpret_cast<const volatile UnitInfo*>(uqueue + k);
+      if (!qe->valid) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(UEMPTY(k));
+        break;
+      }
+      const int T = qe->T, npt = qe->npt, tail_valid = qe->tail_valid, n = qe->n;
+      bool row_ok;
+      uint64_t anc;
+      {
+        const int m0 = qe->rt * p.rows_per_tile;
+        row_ok = r < p.rows_per_tile && (m0 + r) < n * G;
+        anc = row_ok ? p.anc[qe->o0 + (m0 + r) / G] : 0ull;
+      }
+      const uint32_t obuf = tmem + lane_base + 256 + (uint32_t)((uq & 1) * D);
+      float m_ref = -INFINITY, l = 0.f;
+      for (int t = 0; t < T && ok; ++t) {
+        const int tg = tt + t;
+        if (!__all_sync(kAll, mbar_wait(S_FULL(tg & 1), (tg >> 1) & 1, abort_flag, kWaitNs))) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sbuf = tmem + lane_base + (uint32_t)((tg & 1) * 128);
+        float sv[BN / 2];
+        {
+          uint32_t rr[64];
+          tmem_ld_x64(sbuf + kofs, rr);
+#pragma unroll
+          for (int e = 0; e < 64; ++e) sv[e] = __uint_as_float(rr[e]);
+        }
+        const bool tree = (t == npt);
+        const bool partial = tree || (t == npt - 1 && tail_valid < BN);
+        if (partial) {
+          // tree tile: ancestor bits; last prefix tile: key range
+          const int lim = tree ? min(n, 64) : tail_valid;
+#pragma unroll
+          for (int e = 0; e < 64; ++e) {
+            const int key = kofs + e;
+            bool vis = key < lim;
+            if (tree) vis = vis && ((anc >> (key & 63)) & 1ull);
+            sv[e] = vis ? sv[e] : -INFINITY;
+          }
+        }
+        float mx8[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) mx8[a] = sv[a];
+#pragma unroll
+        for (int e = 8; e < 64; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], sv[e]);
+        float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                         fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        // exchange the half-row maximum with the other half
+        float* xb = xch + (xt & 1) * 256;
+        xb[half * 128 + r] = mx;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(XCH(xt & 1));
+        if (!__all_sync(kAll, mbar_wait(XCH(xt & 1), (xt >> 1) & 1, abort_flag, kWaitNs))) { ok = false; break; }
+        ++xt;
+        mx = fmaxf(mx, xb[(half ^ 1) * 128 + r]);
+        const float m_tile = mx == -INFINITY ? -INFINITY : mx * c2;
+        const float m_new = fmaxf(m_ref, m_tile);
+        const bool first = (m_ref == -INFINITY);
+        const bool need = !first && (m_new > m_ref + kRescaleThreshold);
+        if (__any_sync(kAll, need)) {
+          // the O rows must hold P(t-1) V(t-1) before they are rescaled (t >= 1 here)
+          const int ug = tg - 1;
+          if (!__all_sync(kAll, mbar_wait(O_DONE(ug & 1), (ug >> 1) & 1, abort_flag, kWaitNs))) { ok = false; break; }
+          tc_fence_after();
+          const float alpha = need ? ex2(m_ref - m_new) : 1.f;
+          uint32_t rr[32];
+          const uint32_t oa = obuf + half * (D / 2);
+          tmem_ld_x32(oa, rr);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
+          tmem_st_x32(oa, rr);
+          tmem_ld_x32(oa + 32, rr);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
+          tmem_st_x32(oa + 32, rr);
+          if (need) {
+            l *= alpha;
+            m_ref = m_new;
+          }
+        }
+        if (first) m_ref = m_new;
+        const float nm = m_ref == -INFINITY ? 0.f : -m_ref;   // masked keys: 2^-inf = 0
+        float l8[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) l8[a] = 0.f;
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float p0 = ex2(fmaf(sv[2 * e], c2, nm));
+          const float p1 = ex2(fmaf(sv[2 * e + 1], c2, nm));
+          l8[(2 * e) & 7] += p0;
+          l8[(2 * e + 1) & 7] += p1;
+          pk[e] = pack_bf16(p0, p1);
+        }
+        l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+        tmem_st_x32(sbuf + half * 32, pk);          // P over the S columns, bf16 pairs
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(P_FULL(tg & 1));
+      }
+      // epilogue of the unit: the last P V has landed; the two halves' sums
+      // are added through the next exchange buffer.  A sequence with one
+      // chunk writes its normalised rows directly; otherwise the partial
+      // O_s / l_s (bf16) is staged in 128-byte swizzled boxes (box = half)
+      // once the store warp has released the previous unit's staging, and
+      // each box's barrier is arrived in every path.
+      const int ul = tt + T - 1;
+      const bool direct = p.out != nullptr && qe->nch == 1;
+      bool epi = ok && __all_sync(kAll, mbar_wait(O_DONE(ul & 1), (ul >> 1) & 1, abort_flag, kWaitNs));
+      float lsum = 0.f;
+      if (epi) {
+        tc_fence_after();
+        float* xb = xch + (xt & 1) * 256;
+        xb[half * 128 + r] = l;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(XCH(xt & 1));
+        epi = __all_sync(kAll, mbar_wait(XCH(xt & 1), (xt >> 1) & 1, abort_flag, kWaitNs));
+        ++xt;
+        lsum = l + xb[(half ^ 1) * 128 + r];
+      }
+      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+      uint32_t rv[64];
+      if (epi) tmem_ld_x64(obuf + half * (D / 2), rv);
+      if (epi && direct && row_ok) {
+        const int m = qe->rt * p.rows_per_tile + r;   // query row of the KV head: node m / G, head g G + m % G
+        const int64_t e0 = ((int64_t)(qe->o0 + m / G) * p.Hq + qe->g * G + m % G) * D + half * (D / 2);
+        uint4* ob = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + e0);
+#pragma unroll
+        for (int e8 = 0; e8 < 8; ++e8) {
+          uint4 w4;
+          w4.x = pack_bf16(__uint_as_float(rv[8 * e8 + 0]) * inv, __uint_as_float(rv[8 * e8 + 1]) * inv);
+          w4.y = pack_bf16(__uint_as_float(rv[8 * e8 + 2]) * inv, __uint_as_float(rv[8 * e8 + 3]) * inv);
+          w4.z = pack_bf16(__uint_as_float(rv[8 * e8 + 4]) * inv, __uint_as_float(rv[8 * e8 + 5]) * inv);
+          w4.w = pack_bf16(__uint_as_float(rv[8 * e8 + 6]) * inv, __uint_as_float(rv[8 * e8 + 7]) * inv);
+          ob[e8] = w4;
+        }
+      } else if (epi && !direct) {
+        // this row's half of the partial, straight to its slot
+        uint4* ob = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o_part) +
+                                             partial_slot(qe->s, qe->b, qe->g, qe->rt, r, p.Hkv, p.row_tiles, BM,
+                                                          p.splits) * D + half * (D / 2));
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+          uint4 w4;
+          w4.x = pack_bf16(__uint_as_float(rv[8 * c8 + 0]) * inv, __uint_as_float(rv[8 * c8 + 1]) * inv);
+          w4.y = pack_bf16(__uint_as_float(rv[8 * c8 + 2]) * inv, __uint_as_float(rv[8 * c8 + 3]) * inv);
+          w4.z = pack_bf16(__uint_as_float(rv[8 * c8 + 4]) * inv, __uint_as_float(rv[8 * c8 + 5]) * inv);
+          w4.w = pack_bf16(__uint_as_float(rv[8 * c8 + 6]) * inv, __uint_as_float(rv[8 * c8 + 7]) * inv);
+          ob[c8] = w4;
+        }
+      }
+      tc_fence_before();
+      if (epi && !direct)
+        p.ml_part[partial_slot(qe->s, qe->b, qe->g, qe->rt, r, p.Hkv, p.row_tiles, BM, p.splits)] =
+            make_float2(row_ok ? m_ref : -INFINITY, row_ok ? lsum : 0.f);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(UEMPTY(k));       // done with the queue entry
+      k ^= 1;
+      if (!epi) ok = false;
+      tt += T;
+      ++uq;
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0 && *abort_flag) set_status(p.status, TV_DEV_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------- host
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn_p() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+bool encode_p(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+              const cuuint32_t* box) {
+  EncodeTiledFn fn = encode_fn_p();
+  if (!fn) return false;
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int64_t tcp_units(const AttnParams& p) { return (int64_t)p.splits * p.B * p.Hkv * p.row_tiles; }
+
+cudaError_t launch_attn_tcp(const AttnParams& p, cudaStream_t st) {
+  if (p.d != D || !p.part_bf16 || !p.work_counter) return cudaErrorInvalidValue;
+  CUtensorMap mq, mkc, mvc, mkt, mvt;
+  const cuuint64_t row_bytes = (cuuint64_t)D * 2;
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.Hq, (cuuint64_t)p.R};
+    cuuint64_t strides[2] = {row_bytes, row_bytes * p.Hq};
+    cuuint32_t box[3] = {64, (cuuint32_t)p.G, (cuuint32_t)(BM / p.G)};
+    if (!encode_p(&mq, p.q, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t rows = p.paged ? (cuuint64_t)p.num_pages * p.Hkv * kPageSize
+                                    : (cuuint64_t)p.B * p.Hkv * p.capacity;
+    cuuint64_t dims[2] = {(cuuint64_t)D, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {64, (cuuint32_t)(p.paged ? kPageSize : BN)};
+    if (!encode_p(&mkc, p.k_cache, 2, dims, strides, box) || !encode_p(&mvc, p.v_cache, 2, dims, strides, box))
+      return cudaErrorInvalidValue;
+  }
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)p.Hkv * p.R};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {64, BN};
+    if (!encode_p(&mkt, p.k_tree, 2, dims, strides, box) || !encode_p(&mvt, p.v_tree, 2, dims, strides, box))
+      return cudaErrorInvalidValue;
+  }
+  cudaError_t e = ensure_max_dynamic_smem<tv_attn_tcp_kernel>((int)SMEM);
+  if (e != cudaSuccess) return e;
+  const int64_t units = tcp_units(p);
+  const int grid = (int)(units < num_sms() ? units : num_sms());
+  return launch_dep(tv_attn_tcp_kernel, dim3(grid > 0 ? grid : 1), dim3(kThreads), SMEM, st, p, mq, mkc, mvc, mkt,
+                    mvt);
+}
+
+}  // namespace tv

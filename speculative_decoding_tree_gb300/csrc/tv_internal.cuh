@@ -37,6 +37,7 @@ struct AttnParams {
                              // normalised rows here instead of partials (the merge skips it)
   int out_bf16;
   int32_t* status;
+  unsigned long long* work_counter;   // workspace word of the persistent kernel's work queue
   int B, Hq, Hkv, G, d, R, max_nodes;
   int paged;
   int64_t capacity, num_pages, max_pages, max_prefix;
@@ -193,6 +194,8 @@ cudaError_t ensure_max_dynamic_smem(int bytes) {
 cudaError_t launch_attn_simt(const AttnParams& p, int dtype, cudaStream_t s);
 cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t s);
 cudaError_t launch_attn_tc2(const AttnParams& p, cudaStream_t s);
+cudaError_t launch_attn_tcp(const AttnParams& p, cudaStream_t s);
+int64_t tcp_units(const AttnParams& p);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);
 cudaError_t launch_tree_mask(const int32_t* parents, const int32_t* offs, uint64_t* anc, int32_t* depth,
                              int32_t* status, int B, int R, int max_nodes, cudaStream_t s);

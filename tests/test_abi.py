@@ -80,15 +80,25 @@ def test_grid_limits_refused_on_the_host(L):
     big_batch = _desc(batch=70000, total_rows=70000, max_nodes=1, capacity=64, max_prefix=64)
     assert L.tv_workspace_size(ctypes.byref(big_batch), 0, ctypes.byref(n)) == -6
     assert L.tree_verify_attn(ctypes.byref(big_batch), *([fake] * 10), fake, 1 << 30, fake, None) == -6
-    # 64 KV heads x 1100 chunks of 2048 keys on the tensor-core kernel (16 rows per KV head)
+    # 64 KV heads x 1100 chunks of 2048 keys on the one-CTA tensor-core kernel
+    # (16 rows per KV head; an fp32 output keeps the batch off the persistent kernel)
     many_splits = _desc(batch=2, num_q_heads=256, num_kv_heads=64, head_dim=128, max_nodes=4, total_rows=8,
-                        capacity=2048 * 1100, max_prefix=2048 * 1100)
+                        capacity=2048 * 1100, max_prefix=2048 * 1100, out_f32=1)
     assert tv.tv_attn_plan(_desc(batch=2, num_q_heads=256, num_kv_heads=64, head_dim=128, max_nodes=4,
-                                 total_rows=8, capacity=2048 * 1000, max_prefix=2048 * 1000))["kernel"] == 1
+                                 total_rows=8, capacity=2048 * 1000, max_prefix=2048 * 1000,
+                                 out_f32=1))["kernel"] == 1
     assert L.tv_workspace_size(ctypes.byref(many_splits), 0, ctypes.byref(n)) == -6
     ok_splits = _desc(batch=2, num_q_heads=256, num_kv_heads=64, head_dim=128, max_nodes=4, total_rows=8,
-                      capacity=2048 * 1000, max_prefix=2048 * 1000)
+                      capacity=2048 * 1000, max_prefix=2048 * 1000, out_f32=1)
     assert L.tv_workspace_size(ctypes.byref(ok_splits), 0, ctypes.byref(n)) == 0
+    # the persistent batch kernel (bf16 output) counts its work units in 24 bits
+    units_ok = _desc(batch=2, num_q_heads=256, num_kv_heads=64, head_dim=128, max_nodes=4, total_rows=8,
+                     capacity=2048 * 1100, max_prefix=2048 * 1100)
+    assert tv.tv_attn_plan(units_ok)["kernel"] == 3
+    assert L.tv_workspace_size(ctypes.byref(units_ok), 0, ctypes.byref(n)) == 0
+    too_many_units = _desc(batch=2, num_q_heads=256, num_kv_heads=64, head_dim=128, max_nodes=4, total_rows=8,
+                           capacity=2048 * 140000, max_prefix=2048 * 140000)
+    assert L.tv_workspace_size(ctypes.byref(too_many_units), 0, ctypes.byref(n)) == -6
     many_rows = _desc(batch=2000, max_nodes=64, total_rows=66000, capacity=64, max_prefix=32)
     assert L.tv_workspace_size(ctypes.byref(many_rows), 0, ctypes.byref(n)) == 0   # attention alone is fine
     args = [fake] * 15
@@ -133,6 +143,13 @@ def test_workspace_and_plan(L):
     assert tv.tv_attn_plan(_desc(max_nodes=2, total_rows=2))["kernel"] == 0   # 8 rows per KV head
     g3 = tv.tv_attn_plan(_desc(num_q_heads=24))                               # G = 3: 126-row tiles
     assert g3["kernel"] == 2 and g3["rows_per_tile"] == 126
+    # batches: the persistent kernel on head_dim 128 with a bf16 output, else one CTA per tile
+    bd = dict(batch=4, head_dim=128, max_nodes=64, total_rows=200, page_size=16, num_pages=2000, capacity=8192,
+              max_prefix=8000)
+    assert tv.tv_attn_plan(_desc(**bd))["kernel"] == 3
+    assert tv.tv_attn_plan(_desc(**bd))["grid_ctas"] <= 1024
+    assert tv.tv_attn_plan(_desc(**dict(bd, out_f32=1)))["kernel"] == 1
+    assert tv.tv_attn_plan(_desc(**dict(bd, head_dim=256)))["kernel"] == 1
 
 
 def test_sampled_rejects_bad_temperature(L):
