@@ -108,7 +108,7 @@ def measured_peaks():
 
 # sources the split kernels are built from: the recorded DRAM traffic holds
 # only while none of them has changed
-SPLIT_SOURCES = ("tc_ptx.cuh", "tv_internal.cuh", "tv_attn_tc.cu", "tv_attn_tc2.cu", "tv_attn_simt.cu")
+SPLIT_SOURCES = ("tc_ptx.cuh", "tv_internal.cuh", "tv_attn_tc.cu", "tv_attn_tc2.cu", "tv_attn_tcp.cu", "tv_attn_simt.cu")
 
 
 def kernel_source_hash():

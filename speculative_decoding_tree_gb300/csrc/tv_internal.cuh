@@ -73,7 +73,7 @@ struct MergeParams {
   int64_t max_prefix, capacity;
   int chunk, tree_tile, splits;
   int early_reads;           // launched right after the split pass of the same call
-  int slab_rows;             // rows per merge CTA (2..16, even, <= tile_stride)
+  int slab_rows;             // rows per merge CTA (2..32, a power of two, <= tile_stride)
   int batch_splits;          // splits gathered into shared memory at once
 };
 

@@ -25,6 +25,9 @@ namespace {
 using namespace tc;
 
 constexpr int kMergeThreads = 256;
+// most rows one merge CTA takes: 32 at head_dim 128 (a batch's many small
+// tiles: fewer CTAs), 16 otherwise
+__host__ __device__ constexpr int max_slab_rows(int d) { return d <= 128 ? 32 : 16; }
 constexpr uint64_t kMergeWaitNs = 1000000000ull;
 
 __device__ __forceinline__ float4 load4(const float* row, int c) {
@@ -42,7 +45,7 @@ __global__ __launch_bounds__(kMergeThreads) void merge_slab_kernel(MergeParams p
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bar;
   __shared__ int abort_flag;
-  __shared__ float s_m[16], s_l[16], s_keep[16];
+  __shared__ float s_m[max_slab_rows(D)], s_l[max_slab_rows(D)], s_keep[max_slab_rows(D)];
   const int tid = threadIdx.x;
   const int RS = p.slab_rows, SB = p.batch_splits, S = p.splits;
   PT* so = reinterpret_cast<PT*>(smem);                                              // [RS][SB][D]
@@ -100,7 +103,7 @@ __global__ __launch_bounds__(kMergeThreads) void merge_slab_kernel(MergeParams p
 
   constexpr int C4 = D / 4;                         // float4 columns per row
   const int items = rows * C4;
-  constexpr int kMaxItems = 16 * C4 / kMergeThreads + 1;   // slab_rows <= 16
+  constexpr int kMaxItems = max_slab_rows(D) * C4 / kMergeThreads + 1;
   float4 acc[kMaxItems];
 #pragma unroll
   for (int k = 0; k < kMaxItems; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -220,9 +223,10 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t s) {
 
 void merge_shape(int tiles, int tile_stride, int d, int esize, int splits, int sms, int* slab_rows,
                  int* batch_splits) {
-  // the largest slab (16, 8, 4 or 2 rows) that still gives every SM a CTA,
+  // the largest slab (32 rows at head_dim 128, else 16; then 8, 4, 2) that
+  // still gives every SM a CTA,
   // then as many splits per batch as about 100 KB of shared memory holds
-  int rs = 16;
+  int rs = max_slab_rows(d);
   while (rs > 2 && (rs > tile_stride || (int64_t)tiles * ((tile_stride + rs - 1) / rs) < sms)) rs >>= 1;
   const int per_split = rs * (d * esize + 8 + 4);
   int sb = (100 * 1024) / per_split;
