@@ -95,15 +95,13 @@ int make_plan(const tv_desc* d, Plan* p) {
   }
   int row_tiles = (d->max_nodes * G + rows_per_tile - 1) / rows_per_tile;
   // two or more 128-row tiles per KV head: CTA pairs (cta_group::2) share
-  // each K/V tile -- for one sequence.  In a batch the trees differ in size
-  // and a pair whose tree fills one tile leaves its peer idle; one CTA per
-  // tile is faster there even though the larger trees read their K/V twice
-  // (the batched workload: 137 against 159 us)
+  // each K/V tile -- for one sequence
   const bool pairs = tc && row_tiles >= 2 && d->batch == 1;
-  // a batch on head_dim 128 with a bf16 output: one persistent CTA per SM
-  // takes (sequence, KV head, row tile, chunk) units from a work counter
+  // a batch on head_dim 128 with a bf16 output: persistent CTA pairs, one CTA
+  // per SM, take (sequence, KV head, pair of row tiles, chunk) units from a
+  // work counter and share each K/V tile through multicast loads
   const bool persist = tc && d->batch > 1 && d->head_dim == 128 && !d->out_f32;
-  const int launched_tiles = pairs ? 2 * ((row_tiles + 1) / 2) : row_tiles;
+  const int launched_tiles = (pairs || persist) ? 2 * ((row_tiles + 1) / 2) : row_tiles;
   int64_t units = (int64_t)d->batch * d->num_kv_heads * launched_tiles;
   int64_t sms = num_sms();
   int64_t L = d->max_prefix;
@@ -147,7 +145,7 @@ int make_plan(const tv_desc* d, Plan* p) {
   p->pub.chunk = (int)chunk;
   p->pub.row_tiles = row_tiles;
   p->pub.rows_per_tile = rows_per_tile;
-  p->pub.grid_ctas = (int)(persist ? (grid < sms ? grid : sms) : grid);
+  p->pub.grid_ctas = (int)(persist ? (grid < 2 * (sms / 2) ? grid : 2 * (sms / 2)) : grid);
   p->counter_bytes = persist ? 256 : 0;
   // partials are tile-major: every (split, sequence, KV head, row tile) owns
   // tile_stride rows (128 for the tensor-core kernel, whose epilogue stores

@@ -1,14 +1,22 @@
 // tcgen05 split-KV tree-verify attention for batches of sequences (bf16
-// Q/K/V, head_dim 128, bf16 output): one persistent CTA per SM.
+// Q/K/V, head_dim 128, bf16 output): persistent CTA pairs, one CTA per SM.
 //
 // The arithmetic is the one-CTA kernel's (flash-decode with a tree mask,
 // "ADR-037 — EAGLE-3 with dynamic tree port", phase rows E1.1-E1.5 and
-// E4b.6, the dk128 retrofit): a work unit is (sequence b, KV head g, query
-// row tile rt, key chunk s); its keys are the chunk's prefix positions in
-// 128-key tiles and, in the sequence's last chunk, one tile of tree keys
-// masked by each row's ancestor bits; the unit leaves a normalised partial
-// O_s / l_s (bf16) with its running maximum and sum for the merge, or the
-// final rows when the sequence has one chunk.
+// E4b.6, the dk128 retrofit): a work unit is (sequence b, KV head g, a pair
+// of query row tiles, key chunk s); CTA r of a two-CTA cluster computes row
+// tile 2 p + r of the pair p.  The unit's keys are the chunk's prefix
+// positions in 128-key tiles and, in the sequence's last chunk, one tile of
+// tree keys masked by each row's ancestor bits; each row tile leaves a
+// normalised partial O_s / l_s (bf16) with its running maximum and sum for
+// the merge, or the final rows when the sequence has one chunk.
+//
+// The two CTAs of a pair read the same K/V tiles, so each loads half of
+// every tile (its pages, or its 64 keys) with TMA multicast into both CTAs'
+// shared memory.  On a paged cache a 128-key tile is sixteen 16-row boxes
+// and the TMA unit's cost per box sets this path's pace: the pair halves the
+// boxes each SM issues.  A tree whose rows fill one tile leaves the second
+// CTA's rows empty; it still takes its half of the loads.
 //
 // In a batch the sequences have different prefix lengths and tree sizes, so
 // a grid of one CTA per unit runs in uneven waves and pays the CTA's setup
@@ -26,9 +34,10 @@
 //               into one of two 128-column buffers, O += P V into one of two
 //               O buffers (alternating by unit, so that a unit's epilogue
 //               can read its O while the next unit accumulates).
-//   warp 2      scheduler (lane 0): takes unit numbers from the counter,
-//               decodes them (lengths, offsets, chunk bounds) and hands them
-//               through a two-entry queue in shared memory to the others.
+//   warp 2      scheduler (lane 0 of the pair's first CTA): takes unit
+//               numbers from the counter, decodes them (lengths, offsets,
+//               chunk bounds) and hands them through a two-entry queue in
+//               both CTAs' shared memory to the other roles of both.
 //   warps 3-10  softmax (two threads per query row, each half of a tile's
 //               keys), then each unit's epilogue, which writes the partial
 //               rows straight from registers.
@@ -38,8 +47,12 @@
 // (1 s); on a timeout the CTA raises TV_DEV_TIMEOUT and every role leaves
 // its loop.
 //
+// Slots are released to the producers when both CTAs' products are done
+// with them (each MMA thread's commit arrives on EMPTY in both CTAs), and the
+// pair meets at a cluster barrier before it exits.
+//
 // The work counter needs no zeroing: its word holds a tag (the low 40 bits
-// of the launch's %gridid) above a 24-bit count.  Every CTA first raises the
+// of the launch's %gridid) above a 24-bit count.  Every pair first raises the
 // word to (tag, 0) with an atomic maximum (an earlier launch's word has a
 // smaller tag; memory never written by a launch, with a larger one, is
 // replaced by compare-and-swap) and only then takes numbers with atomic adds.
@@ -72,12 +85,13 @@ constexpr int kSoftmaxWarps = 8;
 constexpr uint64_t kWaitNs = 1000000000ull;
 constexpr float kRescaleThreshold = 8.0f;       // rescale O when the max grows by > 2^8
 constexpr int kUnitSlots = 2;                   // the unit queue
-constexpr int kUnitReaders = 2 + kSoftmaxWarps; // producer, MMA lane, softmax warps
+constexpr int kUnitReaders = 2 * (2 + kSoftmaxWarps);   // both CTAs' producer, MMA lane, softmax warps
+constexpr int KH = BN / 2;                      // keys of a tile each CTA of the pair loads
 
 // barrier numbers
 constexpr int B_FULL = 0, B_EMPTY = NS, B_QFULL = 2 * NS, B_QEMPTY = B_QFULL + 1, B_SFULL = B_QEMPTY + 1,
               B_PFULL = B_SFULL + 2, B_ODONE = B_PFULL + 2, B_XCH = B_ODONE + 2, B_TAIL = B_XCH + 2,
-              B_FIN = B_TAIL + 1, B_UFULL = B_FIN + 1, B_UEMPTY = B_UFULL + kUnitSlots,
+              B_FIN = B_TAIL + 2, B_UFULL = B_FIN + 1, B_UEMPTY = B_UFULL + kUnitSlots,
               NBARS = B_UEMPTY + kUnitSlots;
 static_assert(NBARS * 8 + 8 <= 256, "barriers overflow the header");
 
@@ -119,18 +133,21 @@ __device__ __forceinline__ void arm_counter(unsigned long long* cnt, unsigned lo
   }
 }
 
-// Unit u (chunk-major numbering) with everything the roles need; false when
-// it has no rows (tile past the tree's rows, invalid offsets) or no keys
-// (chunk past the sequence's prefix).
-// (Unit numbers stay below 2^24, which the host checks, so 32-bit
-// arithmetic decodes them.)
+__host__ __device__ __forceinline__ int row_pairs(int row_tiles) { return (row_tiles + 1) / 2; }
+
+// Unit u (chunk-major numbering; row tiles in pairs) with everything the
+// roles need (rt is the pair's first row tile); false when it has no rows
+// (tiles past the tree's rows, invalid offsets) or no keys (chunk past the
+// sequence's prefix).  (Unit numbers stay below 2^24, which the host
+// checks, so 32-bit arithmetic decodes them.)
 __device__ bool decode_unit(const AttnParams& p, int u, UnitInfo& ui) {
-  const int per_s = p.B * p.Hkv * p.row_tiles;
+  const int rp = row_pairs(p.row_tiles);
+  const int per_s = p.B * p.Hkv * rp;
   const int s = u / per_s;
   const int rem = u - s * per_s;
-  const int b = rem / (p.Hkv * p.row_tiles);
-  const int g = (rem / p.row_tiles) % p.Hkv;
-  const int rt = rem % p.row_tiles;
+  const int b = rem / (p.Hkv * rp);
+  const int g = (rem / rp) % p.Hkv;
+  const int rt = 2 * (rem % rp);
   int o0 = 0, n = 1;
   if (!seq_rows(p.node_offsets, b, p.R, p.max_nodes, p.status, &o0, &n)) return false;
   if (rt * p.rows_per_tile >= n * p.G) return false;
@@ -156,7 +173,7 @@ __device__ bool decode_unit(const AttnParams& p, int u, UnitInfo& ui) {
   return true;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_kc, const __grid_constant__ CUtensorMap tm_vc,
                    const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_vt) {
@@ -174,7 +191,8 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   auto FULL = [&](int i) { return bar(B_FULL + i); };
   auto EMPTY = [&](int i) { return bar(B_EMPTY + i); };
-  const uint32_t Q_FULL = bar(B_QFULL), Q_EMPTY = bar(B_QEMPTY), TAIL = bar(B_TAIL), FIN = bar(B_FIN);
+  const uint32_t Q_FULL = bar(B_QFULL), Q_EMPTY = bar(B_QEMPTY), FIN = bar(B_FIN);
+  auto TAIL = [&](int i) { return bar(B_TAIL + i); };
   auto S_FULL = [&](int i) { return bar(B_SFULL + i); };
   auto P_FULL = [&](int i) { return bar(B_PFULL + i); };
   auto O_DONE = [&](int i) { return bar(B_ODONE + i); };
@@ -192,7 +210,7 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(FULL(i), 1);
-      mbar_init(EMPTY(i), 1);
+      mbar_init(EMPTY(i), 2);                       // both CTAs' MMAs are done with the slot
     }
     mbar_init(Q_FULL, 1);
     mbar_init(Q_EMPTY, 1);
@@ -202,7 +220,8 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       mbar_init(O_DONE(i), 1);
       mbar_init(XCH(i), kSoftmaxWarps);
     }
-    mbar_init(TAIL, 1);
+    mbar_init(TAIL(0), 1);
+    mbar_init(TAIL(1), 1);
     mbar_init(FIN, 1);
     for (int i = 0; i < kUnitSlots; ++i) {
       mbar_init(UFULL(i), 1);
@@ -234,50 +253,55 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();                               // the peer's barriers are ready before any remote arrive
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   dep_wait();
   dep_launch();
 
   const int G = p.G;
-  if (warp == 2 && lane == 0) {
+  const uint32_t rank = cluster_ctarank();          // 0: the pair's first CTA
+  constexpr uint16_t kPair = 3;                     // multicast to both CTAs
+  // a queue entry is handed back to the scheduler (in CTA 0) once read
+  auto release_entry = [&](int kq) {
+    if (rank == 0) mbar_arrive(UEMPTY(kq));
+    else mbar_arrive_cluster_release(map_to_cta(UEMPTY(kq), 0));
+  };
+  if (warp == 2 && lane == 0 && rank == 0) {
     // ============================================================ scheduler
-    {
-      const int U = p.splits * p.B * p.Hkv * p.row_tiles;
-      const unsigned long long tag = launch_tag();
-      arm_counter(p.work_counter, tag);
-      auto next = [&]() -> int {
-        return (int)gridDim.x + (int)(atomicAdd(p.work_counter, 1ull) & 0xFFFFFFull);
-      };
-      int u = blockIdx.x;
-      int k = 0, pushes = 0;
-      while (true) {
-        UnitInfo ui;
-        ui.valid = 0;
-        while (u < U && !decode_unit(p, u, ui)) u = next();
-        if (pushes >= kUnitSlots &&
-            !mbar_wait(UEMPTY(k), ((pushes / kUnitSlots) - 1) & 1, abort_flag, kWaitNs))
-          break;                                    // aborted: every role leaves on the flag
-        volatile UnitInfo* qe = reinterpret_cast<volatile UnitInfo*>(uqueue + k);
-        qe->valid = ui.valid;
-        qe->b = ui.b;
-        qe->g = ui.g;
-        qe->rt = ui.rt;
-        qe->s = ui.s;
-        qe->o0 = ui.o0;
-        qe->n = ui.n;
-        qe->nch = ui.nch;
-        qe->npt = ui.npt;
-        qe->T = ui.T;
-        qe->tail_valid = ui.tail_valid;
-        qe->k_begin = ui.k_begin;
-        qe->k_end = ui.k_end;
-        mbar_arrive(UFULL(k));
-        ++pushes;
-        k ^= 1;
-        if (!ui.valid) break;
-        u = next();
+    const int U = p.splits * p.B * p.Hkv * row_pairs(p.row_tiles);
+    const int pairs = (int)(gridDim.x / 2);
+    const unsigned long long tag = launch_tag();
+    arm_counter(p.work_counter, tag);
+    auto next = [&]() -> int { return pairs + (int)(atomicAdd(p.work_counter, 1ull) & 0xFFFFFFull); };
+    int u = (int)(blockIdx.x / 2);
+    int k = 0, pushes = 0;
+    while (true) {
+      UnitInfo ui;
+      ui.valid = 0;
+      while (u < U && !decode_unit(p, u, ui)) u = next();
+      if (pushes >= kUnitSlots &&
+          !mbar_wait_cluster(UEMPTY(k), ((pushes / kUnitSlots) - 1) & 1, abort_flag, kWaitNs))
+        break;                                      // aborted: every role leaves on the flag
+      // the entry, word by word, into this CTA's queue and the peer's
+      const uint32_t qa = smem_u32(uqueue + k), qr = map_to_cta(qa, 1);
+      const uint32_t words[16] = {(uint32_t)ui.valid, (uint32_t)ui.b, (uint32_t)ui.g, (uint32_t)ui.rt,
+                                  (uint32_t)ui.s, (uint32_t)ui.o0, (uint32_t)ui.n, (uint32_t)ui.nch,
+                                  (uint32_t)ui.npt, (uint32_t)ui.T, (uint32_t)ui.tail_valid, 0u,
+                                  (uint32_t)ui.k_begin, (uint32_t)((uint64_t)ui.k_begin >> 32),
+                                  (uint32_t)ui.k_end, (uint32_t)((uint64_t)ui.k_end >> 32)};
+      volatile uint32_t* ql = reinterpret_cast<volatile uint32_t*>(uqueue + k);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        ql[i] = words[i];
+        st_cluster_u32(qr + 4 * i, words[i]);
       }
+      mbar_arrive(UFULL(k));
+      mbar_arrive_cluster_release(map_to_cta(UFULL(k), 1));
+      ++pushes;
+      k ^= 1;
+      if (!ui.valid) break;
+      u = next();
     }
   } else if (warp == 0) {
     // ============================================================ producer
@@ -285,15 +309,15 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     bool ok = true;
     const int oob_row = p.paged ? (int)(p.num_pages * p.Hkv * kPageSize) : 0;
     while (ok) {
-      if (!__all_sync(kAll, mbar_wait(UFULL(k), (uq / kUnitSlots) & 1, abort_flag, kWaitNs))) break;
+      if (!__all_sync(kAll, mbar_wait_cluster(UFULL(k), (uq / kUnitSlots) & 1, abort_flag, kWaitNs))) break;
       const volatile UnitInfo* qe = reinterpret_cast<const volatile UnitInfo*>(uqueue + k);
       if (!qe->valid) {
         __syncwarp();
-        if (lane == 0) mbar_arrive(UEMPTY(k));
+        if (lane == 0) release_entry(k);
         break;
       }
       const int b = qe->b, g = qe->g, npt = qe->npt, T = qe->T, tail_valid = qe->tail_valid, o0 = qe->o0;
-      const int q_node = o0 + qe->rt * p.rows_per_tile / G;   // the Q tile's first node
+      const int q_node = o0 + (qe->rt + (int)rank) * p.rows_per_tile / G;   // this CTA's Q tile's first node
       const int64_t k_begin = qe->k_begin, k_end = qe->k_end;
       // The unit's Q tile replaces the previous unit's once that unit's QK
       // products are done (Q_EMPTY).  It is loaded just before the unit's
@@ -345,15 +369,22 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
             ok = false;
             break;
           }
+          // Each CTA loads half of the tile into both CTAs' slots: keys
+          // 64 r .. 64 r + 63 (pages 4 r .. 4 r + 3 on a paged cache).  The
+          // slot's barrier expects the whole tile's bytes; the peer's half
+          // may land before this thread's expect_tx, which the transaction
+          // count allows within a phase.
           uint8_t* dst = ring + slot * SLOT_BYTES;
-          const uint32_t fb = tail_fix ? TAIL : FULL(slot);
+          const uint32_t fb = tail_fix ? TAIL(tail_uses & 1) : FULL(slot);
           if (tree || !p.paged) {
             if (lane == 0) {
               mbar_expect_tx(fb, SLOT_BYTES);
               const CUtensorMap* m = tree ? (kind == 0 ? &tm_kt : &tm_vt) : (kind == 0 ? &tm_kc : &tm_vc);
-              const int64_t row = tree ? (int64_t)g * p.R + o0
-                                       : ((int64_t)b * p.Hkv + g) * p.capacity + k_begin + (int64_t)tile * BN;
-              for (int bx = 0; bx < 2; ++bx) tma_load_2d(smem_u32(dst + bx * BOX_BYTES), m, fb, bx * 64, (int)row);
+              const int64_t row = (tree ? (int64_t)g * p.R + o0
+                                        : ((int64_t)b * p.Hkv + g) * p.capacity + k_begin + (int64_t)tile * BN) +
+                                  KH * rank;
+              for (int bx = 0; bx < 2; ++bx)
+                tma_load_2d_mc(smem_u32(dst + bx * BOX_BYTES + KH * rank * 128), m, fb, bx * 64, (int)row, kPair);
             }
           } else {
             const CUtensorMap* m = kind == 0 ? &tm_kc : &tm_vc;
@@ -361,14 +392,18 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
             const int npages = __popc(__ballot_sync(kAll, my_row >= 0));
             if (lane == 0) mbar_expect_tx(fb, (uint32_t)npages * 2u * (kPageSize * 128u));
             __syncwarp();
-            if (my_row >= 0)
+            if (my_row >= 0 && (lane >> 2) == (int)rank)
               for (int bx = 0; bx < 2; ++bx)
-                tma_load_2d(smem_u32(dst + bx * BOX_BYTES + lane * kPageSize * 128), m, fb, bx * 64, my_row);
+                tma_load_2d_mc(smem_u32(dst + bx * BOX_BYTES + lane * kPageSize * 128), m, fb, bx * 64, my_row,
+                               kPair);
           }
           __syncwarp();
           if (tail_fix) {
-            // the chunk's rows past the prefix end become zeros before the MMA reads them
-            if (!__all_sync(kAll, mbar_wait(TAIL, tail_uses & 1, abort_flag, kWaitNs))) {
+            // the chunk's rows past the prefix end become zeros before the
+            // MMA reads them (both halves have landed: the TAIL phase counts
+            // the whole tile).  Two TAIL barriers alternate: the peer cannot
+            // start a second tail tile before this CTA has passed the first.
+            if (!__all_sync(kAll, mbar_wait(TAIL(tail_uses & 1), (tail_uses >> 1) & 1, abort_flag, kWaitNs))) {
               ok = false;
               break;
             }
@@ -386,7 +421,7 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(UEMPTY(k));       // done with the queue entry
+      if (lane == 0) release_entry(k);             // done with the queue entry
       k ^= 1;
       ++uq;
     }
@@ -405,11 +440,11 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       int j = 0, tt = 0, uq = 0, k = 0;
       bool ok = true;
       while (ok) {
-        if (!mbar_wait(UFULL(k), (uq / kUnitSlots) & 1, abort_flag, kWaitNs)) break;
+        if (!mbar_wait_cluster(UFULL(k), (uq / kUnitSlots) & 1, abort_flag, kWaitNs)) break;
         const int T = reinterpret_cast<const volatile UnitInfo*>(uqueue + k)->valid
                           ? reinterpret_cast<const volatile UnitInfo*>(uqueue + k)->T
                           : 0;
-        mbar_arrive(UEMPTY(k));                     // only T is needed, and it is read
+        release_entry(k);                           // only T is needed, and it is read
         k ^= 1;
         if (T == 0) break;
         const uint32_t obuf = tmem + 256 + (uint32_t)((uq & 1) * D);
@@ -429,7 +464,7 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
               const uint64_t bd = smem_desc(kaddr + (kk >> 2) * BOX_BYTES + (kk & 3) * 32, 16, 1024, 2);
               mma_ss(sbuf, a, bd, ID_QK, kk > 0 ? 1u : 0u);
             }
-            mma_commit(EMPTY(slot));
+            mma_commit_mc(EMPTY(slot), kPair);
             mma_commit(S_FULL(tg & 1));
             if (t == T - 1) mma_commit(Q_EMPTY);    // the unit's last product that reads Q
             ++j;
@@ -448,7 +483,7 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
               const uint64_t bd = smem_desc(vaddr + kk * (16 * 128), BOX_BYTES, 1024, 2);
               mma_ts(obuf, pbuf + kk * 8, bd, ID_PV, (u > 0 || kk > 0) ? 1u : 0u);
             }
-            mma_commit(EMPTY(slot));
+            mma_commit_mc(EMPTY(slot), kPair);
             mma_commit(O_DONE(ug & 1));
             ++j;
           }
@@ -473,21 +508,22 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     int tt = 0, xt = 0, uq = 0, k = 0;
     bool ok = true;
     while (ok) {
-      if (!__all_sync(kAll, mbar_wait(UFULL(k), (uq / kUnitSlots) & 1, abort_flag, kWaitNs))) break;
+      if (!__all_sync(kAll, mbar_wait_cluster(UFULL(k), (uq / kUnitSlots) & 1, abort_flag, kWaitNs))) break;
       // the entry stays valid until this warp arrives on UEMPTY at the end of
       // the unit: fields the epilogue needs are read there again (fewer live
       // registers through the tile loop)
       const volatile UnitInfo* qe = reinterpret_cast<const volatile UnitInfo*>(uqueue + k);
       if (!qe->valid) {
         __syncwarp();
-        if (lane == 0) mbar_arrive(UEMPTY(k));
+        if (lane == 0) release_entry(k);
         break;
       }
       const int T = qe->T, npt = qe->npt, tail_valid = qe->tail_valid, n = qe->n;
+      const int my_rt = qe->rt + (int)rank;         // this CTA's row tile of the pair
       bool row_ok;
       uint64_t anc;
       {
-        const int m0 = qe->rt * p.rows_per_tile;
+        const int m0 = my_rt * p.rows_per_tile;
         row_ok = r < p.rows_per_tile && (m0 + r) < n * G;
         anc = row_ok ? p.anc[qe->o0 + (m0 + r) / G] : 0ull;
       }
@@ -586,6 +622,9 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       // each box's barrier is arrived in every path.
       const int ul = tt + T - 1;
       const bool direct = p.out != nullptr && qe->nch == 1;
+      // the pair's second tile may lie past the tree's rows (or past the
+      // last row tile): it computes on zeros and writes nothing
+      const bool tile_live = my_rt < p.row_tiles && my_rt * p.rows_per_tile < qe->n * G;
       bool epi = ok && __all_sync(kAll, mbar_wait(O_DONE(ul & 1), (ul >> 1) & 1, abort_flag, kWaitNs));
       float lsum = 0.f;
       if (epi) {
@@ -602,7 +641,7 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       uint32_t rv[64];
       if (epi) tmem_ld_x64(obuf + half * (D / 2), rv);
       if (epi && direct && row_ok) {
-        const int m = qe->rt * p.rows_per_tile + r;   // query row of the KV head: node m / G, head g G + m % G
+        const int m = my_rt * p.rows_per_tile + r;   // query row of the KV head: node m / G, head g G + m % G
         const int64_t e0 = ((int64_t)(qe->o0 + m / G) * p.Hq + qe->g * G + m % G) * D + half * (D / 2);
         uint4* ob = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + e0);
 #pragma unroll
@@ -614,10 +653,10 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
           w4.w = pack_bf16(__uint_as_float(rv[8 * e8 + 6]) * inv, __uint_as_float(rv[8 * e8 + 7]) * inv);
           ob[e8] = w4;
         }
-      } else if (epi && !direct) {
+      } else if (epi && !direct && tile_live) {
         // this row's half of the partial, straight to its slot
         uint4* ob = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o_part) +
-                                             partial_slot(qe->s, qe->b, qe->g, qe->rt, r, p.Hkv, p.row_tiles, BM,
+                                             partial_slot(qe->s, qe->b, qe->g, my_rt, r, p.Hkv, p.row_tiles, BM,
                                                           p.splits) * D + half * (D / 2));
 #pragma unroll
         for (int c8 = 0; c8 < 8; ++c8) {
@@ -630,11 +669,11 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         }
       }
       tc_fence_before();
-      if (epi && !direct)
-        p.ml_part[partial_slot(qe->s, qe->b, qe->g, qe->rt, r, p.Hkv, p.row_tiles, BM, p.splits)] =
+      if (epi && !direct && tile_live)
+        p.ml_part[partial_slot(qe->s, qe->b, qe->g, my_rt, r, p.Hkv, p.row_tiles, BM, p.splits)] =
             make_float2(row_ok ? m_ref : -INFINITY, row_ok ? lsum : 0.f);
       __syncwarp();
-      if (lane == 0) mbar_arrive(UEMPTY(k));       // done with the queue entry
+      if (lane == 0) release_entry(k);             // done with the queue entry
       k ^= 1;
       if (!epi) ok = false;
       tt += T;
@@ -645,6 +684,9 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   // ---------------------------------------------------------------- teardown
   tc_fence_before();
   __syncthreads();
+  // neither CTA leaves while the peer may still write into its shared memory
+  // (multicast copies, commits, queue entries)
+  cluster_sync_all();
   if (tid == 0 && *abort_flag) set_status(p.status, TV_DEV_TIMEOUT);
   if (warp == 1) {
     tc_fence_after();
@@ -686,7 +728,7 @@ bool encode_p(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
 
 }  // namespace
 
-int64_t tcp_units(const AttnParams& p) { return (int64_t)p.splits * p.B * p.Hkv * p.row_tiles; }
+int64_t tcp_units(const AttnParams& p) { return (int64_t)p.splits * p.B * p.Hkv * row_pairs(p.row_tiles); }
 
 cudaError_t launch_attn_tcp(const AttnParams& p, cudaStream_t st) {
   if (p.d != D || !p.part_bf16 || !p.work_counter) return cudaErrorInvalidValue;
@@ -703,23 +745,23 @@ cudaError_t launch_attn_tcp(const AttnParams& p, cudaStream_t st) {
                                     : (cuuint64_t)p.B * p.Hkv * p.capacity;
     cuuint64_t dims[2] = {(cuuint64_t)D, rows};
     cuuint64_t strides[1] = {row_bytes};
-    cuuint32_t box[2] = {64, (cuuint32_t)(p.paged ? kPageSize : BN)};
+    cuuint32_t box[2] = {64, (cuuint32_t)(p.paged ? kPageSize : KH)};
     if (!encode_p(&mkc, p.k_cache, 2, dims, strides, box) || !encode_p(&mvc, p.v_cache, 2, dims, strides, box))
       return cudaErrorInvalidValue;
   }
   {
     cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)p.Hkv * p.R};
     cuuint64_t strides[1] = {row_bytes};
-    cuuint32_t box[2] = {64, BN};
+    cuuint32_t box[2] = {64, KH};
     if (!encode_p(&mkt, p.k_tree, 2, dims, strides, box) || !encode_p(&mvt, p.v_tree, 2, dims, strides, box))
       return cudaErrorInvalidValue;
   }
   cudaError_t e = ensure_max_dynamic_smem<tv_attn_tcp_kernel>((int)SMEM);
   if (e != cudaSuccess) return e;
-  const int64_t units = tcp_units(p);
-  const int grid = (int)(units < num_sms() ? units : num_sms());
-  return launch_dep(tv_attn_tcp_kernel, dim3(grid > 0 ? grid : 1), dim3(kThreads), SMEM, st, p, mq, mkc, mvc, mkt,
-                    mvt);
+  const int64_t units = tcp_units(p);                   // pair units
+  const int64_t pairs = num_sms() / 2;
+  const int grid = 2 * (int)(units < pairs ? (units > 0 ? units : 1) : pairs);
+  return launch_dep(tv_attn_tcp_kernel, dim3(grid), dim3(kThreads), SMEM, st, p, mq, mkc, mvc, mkt, mvt);
 }
 
 }  // namespace tv

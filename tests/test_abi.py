@@ -148,6 +148,7 @@ def test_workspace_and_plan(L):
               max_prefix=8000)
     assert tv.tv_attn_plan(_desc(**bd))["kernel"] == 3
     assert tv.tv_attn_plan(_desc(**bd))["grid_ctas"] <= 1024
+    assert tv.tv_attn_plan(_desc(**bd))["grid_ctas"] % 2 == 0                # CTA pairs
     assert tv.tv_attn_plan(_desc(**dict(bd, out_f32=1)))["kernel"] == 1
     assert tv.tv_attn_plan(_desc(**dict(bd, head_dim=256)))["kernel"] == 1
 

@@ -96,3 +96,20 @@ def test_batched_multi_chunk_every_element(batch, seed):
     from speculative_decoding_tree_gb300 import tv_attn_plan
     assert tv_attn_plan(st.desc)["num_splits"] >= 3
     check_step(w, st, oracle.verify_step(w))
+
+
+@pytest.mark.parametrize("paged,hq,seed", [(True, 40, 63), (False, 40, 64), (False, 32, 65)])
+def test_batched_row_tile_pairs(paged, hq, seed):
+    # the batch kernel computes a unit's row tiles in pairs: trees of 1 to 64
+    # nodes at GQA 5 (125-row tiles, 1 to 3 per KV head) leave some pairs
+    # with one live tile, or none past the last; GQA 4 gives 1 or 2 tiles.
+    # Contiguous caches load 64-key halves, paged ones four pages per CTA,
+    # across several key chunks
+    spec = wl.CONFIGS[5].replace(batch=5, hq=hq, prefix=(1, 4500), tree="random:1,64,8", paged=paged,
+                                 vocab=1031, seed=seed)
+    w = workload(spec)
+    st = run(w)
+    from speculative_decoding_tree_gb300 import tv_attn_plan
+    plan = tv_attn_plan(st.desc)
+    assert plan["kernel"] == 3 and plan["grid_ctas"] % 2 == 0
+    check_step(w, st, oracle.verify_step(w))
