@@ -132,7 +132,9 @@ typedef struct tv_desc {
  * counting algorithmic work; filled by tv_attn_plan). */
 typedef struct tv_plan {
   int32_t kernel;         /* 0 = CUDA-core split kernel, 1 = tcgen05 kernel (one CTA per query tile),
-                             2 = tcgen05 kernel on CTA pairs (two query tiles share each K/V tile) */
+                             2 = tcgen05 kernel on CTA pairs (two query tiles share each K/V tile),
+                             3 = persistent tcgen05 kernel on CTA pairs for batches at head_dim 128
+                             (units of (sequence, KV head, two query tiles, chunk) from a counter) */
   int32_t num_splits;     /* KV chunks per (sequence, KV head) at the longest prefix */
   int32_t chunk;          /* keys per chunk (the last chunk of a sequence also takes its tree keys) */
   int32_t row_tiles;      /* query-row tiles per (sequence, KV head) */

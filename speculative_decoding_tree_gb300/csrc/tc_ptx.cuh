@@ -255,6 +255,13 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// execution-only cluster barrier: the arrive does not wait for this thread's
+// earlier memory operations to be performed (a release arrive made every
+// thread of a pair wait for its last global stores at exit)
+__device__ __forceinline__ void cluster_sync_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\nbarrier.cluster.wait.aligned;" ::: "memory");
+}
+
 // arrive on an mbarrier of any CTA of the cluster (release at CTA scope: for
 // hand-offs whose data is tensor memory ordered by the tcgen05 fences)
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr) {

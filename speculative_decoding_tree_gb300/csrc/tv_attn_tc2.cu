@@ -636,10 +636,15 @@ tv_attn_tc2_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   }
 
   // ------------------------------------------------------- teardown (pair)
+  // The leader's last commit (FIN) reaches both CTAs after every earlier
+  // commit: once the peer has seen it, no arrive from the pair's MMAs is in
+  // flight towards its shared memory, and an execution-only cluster barrier
+  // keeps either CTA from leaving before the other is done.
+  if (active && warp == 1 && lane == 0 && rank != 0) mbar_wait(FIN, 0, abort_flag, kWaitNs);
   tc_fence_before();
   __syncthreads();
   if (tid == 0 && *abort_flag) set_status(p.status, TV_DEV_TIMEOUT);
-  cluster_sync_all();                               // neither CTA leaves while the pair still shares state
+  cluster_sync_relaxed();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc_pair(tmem, 512);

@@ -49,13 +49,12 @@
 //
 // Slots are released to the producers when both CTAs' products are done
 // with them (each MMA thread's commit arrives on EMPTY in both CTAs), and the
-// pair meets at a cluster barrier before it exits.
+// pair meets at an execution-only cluster barrier before it exits, once no
+// copy, commit or queue release of either CTA is still on its way.
 //
-// The work counter needs no zeroing: its word holds a tag (the low 40 bits
-// of the launch's %gridid) above a 24-bit count.  Every pair first raises the
-// word to (tag, 0) with an atomic maximum (an earlier launch's word has a
-// smaller tag; memory never written by a launch, with a larger one, is
-// replaced by compare-and-swap) and only then takes numbers with atomic adds.
+// The work counter needs no zeroing: it is a tagged word (launch_tag,
+// arm_counter), raised to this launch's tag by every pair before it takes
+// numbers with atomic adds.
 #include <cuda.h>
 
 #include <climits>
@@ -90,10 +89,10 @@ constexpr int KH = BN / 2;                      // keys of a tile each CTA of th
 
 // barrier numbers
 constexpr int B_FULL = 0, B_EMPTY = NS, B_QFULL = 2 * NS, B_QEMPTY = B_QFULL + 1, B_SFULL = B_QEMPTY + 1,
-              B_PFULL = B_SFULL + 2, B_ODONE = B_PFULL + 2, B_XCH = B_ODONE + 2, B_TAIL = B_XCH + 2,
+              B_PFULL = B_SFULL + 2, B_ODONE = B_PFULL + 2, B_XCH = B_ODONE + 2, B_TAIL = B_XCH + 8,
               B_FIN = B_TAIL + 2, B_UFULL = B_FIN + 1, B_UEMPTY = B_UFULL + kUnitSlots,
               NBARS = B_UEMPTY + kUnitSlots;
-static_assert(NBARS * 8 + 8 <= 256, "barriers overflow the header");
+static_assert(NBARS * 8 + 8 <= 384, "barriers overflow the header");
 
 struct UnitInfo {
   int32_t valid;           // 0: no more units
@@ -103,7 +102,7 @@ struct UnitInfo {
   int64_t k_begin, k_end;  // the chunk's prefix keys
 };
 static_assert(sizeof(UnitInfo) == 64, "unit queue entry");
-constexpr uint32_t kXchOfs = 256;               // [2 parity][2 half][128 rows] floats
+constexpr uint32_t kXchOfs = 384;               // [2 parity][2 half][128 rows] floats
 constexpr uint32_t kQueueOfs = kXchOfs + 2048;
 static_assert(kQueueOfs + kUnitSlots * sizeof(UnitInfo) <= kHeader, "unit queue overflows the header");
 
@@ -118,19 +117,32 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-__device__ __forceinline__ unsigned long long launch_tag() {
-  unsigned long long g;
-  asm volatile("mov.u64 %0, %%gridid;" : "=l"(g));
-  return (g & ((1ull << 40) - 1)) << 24;
+// Packed fp32 pairs (f32x2 arithmetic: one instruction for two lanes of
+// work on the FMA pipes).
+__device__ __forceinline__ uint64_t pk2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
 }
-
-__device__ __forceinline__ void arm_counter(unsigned long long* cnt, unsigned long long tag) {
-  unsigned long long old = atomicMax(cnt, tag);
-  while ((old >> 24) > (tag >> 24)) {               // not an earlier launch's word: replace it
-    const unsigned long long prev = atomicCAS(cnt, old, tag);
-    if (prev == old) break;
-    old = prev;                                     // changed meanwhile (another CTA may have armed it)
-  }
+__device__ __forceinline__ float2 up2(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 __host__ __device__ __forceinline__ int row_pairs(int row_tiles) { return (row_tiles + 1) / 2; }
@@ -196,7 +208,7 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   auto S_FULL = [&](int i) { return bar(B_SFULL + i); };
   auto P_FULL = [&](int i) { return bar(B_PFULL + i); };
   auto O_DONE = [&](int i) { return bar(B_ODONE + i); };
-  auto XCH = [&](int i) { return bar(B_XCH + i); };
+  auto XCH = [&](int q, int i) { return bar(B_XCH + 2 * q + i); };   // row quarter q, parity i
   auto UFULL = [&](int i) { return bar(B_UFULL + i); };
   auto UEMPTY = [&](int i) { return bar(B_UEMPTY + i); };
 
@@ -218,11 +230,11 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       mbar_init(S_FULL(i), 1);
       mbar_init(P_FULL(i), kSoftmaxWarps);
       mbar_init(O_DONE(i), 1);
-      mbar_init(XCH(i), kSoftmaxWarps);
+      for (int q = 0; q < 4; ++q) mbar_init(XCH(q, i), 2);   // the row quarter's two warps
     }
     mbar_init(TAIL(0), 1);
     mbar_init(TAIL(1), 1);
-    mbar_init(FIN, 1);
+    mbar_init(FIN, 2);                              // both CTAs' MMA issuers are done
     for (int i = 0; i < kUnitSlots; ++i) {
       mbar_init(UFULL(i), 1);
       mbar_init(UEMPTY(i), kUnitReaders);
@@ -300,7 +312,12 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       mbar_arrive_cluster_release(map_to_cta(UFULL(k), 1));
       ++pushes;
       k ^= 1;
-      if (!ui.valid) break;
+      if (!ui.valid) {
+        // the last real entry's releases (some remote) land before this CTA
+        // may leave; the entry before it was waited for to push this one
+        if (pushes >= 2) mbar_wait_cluster(UEMPTY(k), ((pushes - 2) / kUnitSlots) & 1, abort_flag, kWaitNs);
+        break;
+      }
       u = next();
     }
   } else if (warp == 0) {
@@ -311,11 +328,7 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     while (ok) {
       if (!__all_sync(kAll, mbar_wait_cluster(UFULL(k), (uq / kUnitSlots) & 1, abort_flag, kWaitNs))) break;
       const volatile UnitInfo* qe = reinterpret_cast<const volatile UnitInfo*>(uqueue + k);
-      if (!qe->valid) {
-        __syncwarp();
-        if (lane == 0) release_entry(k);
-        break;
-      }
+      if (!qe->valid) break;                     // the last entry: nobody waits for its release
       const int b = qe->b, g = qe->g, npt = qe->npt, T = qe->T, tail_valid = qe->tail_valid, o0 = qe->o0;
       const int q_node = o0 + (qe->rt + (int)rank) * p.rows_per_tile / G;   // this CTA's Q tile's first node
       const int64_t k_begin = qe->k_begin, k_end = qe->k_end;
@@ -444,9 +457,9 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         const int T = reinterpret_cast<const volatile UnitInfo*>(uqueue + k)->valid
                           ? reinterpret_cast<const volatile UnitInfo*>(uqueue + k)->T
                           : 0;
+        if (T == 0) break;                          // the last entry: nobody waits for its release
         release_entry(k);                           // only T is needed, and it is read
         k ^= 1;
-        if (T == 0) break;
         const uint32_t obuf = tmem + 256 + (uint32_t)((uq & 1) * D);
         if (!mbar_wait(Q_FULL, uq & 1, abort_flag, kWaitNs)) break;
         tc_fence_after();
@@ -491,8 +504,10 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         tt += T;
         ++uq;
       }
-      // every MMA this thread issued has finished before tensor memory is freed
-      mma_commit(FIN);
+      // every MMA this thread issued has finished before tensor memory is
+      // freed, and (FIN being each issuer's last commit, to both CTAs) no
+      // commit of either issuer is still on its way to this CTA's barriers
+      mma_commit_mc(FIN, kPair);
       mbar_wait(FIN, 0, abort_flag, kWaitNs);
     }
   } else if (warp >= kFirstSoftmaxWarp) {
@@ -513,11 +528,7 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       // the unit: fields the epilogue needs are read there again (fewer live
       // registers through the tile loop)
       const volatile UnitInfo* qe = reinterpret_cast<const volatile UnitInfo*>(uqueue + k);
-      if (!qe->valid) {
-        __syncwarp();
-        if (lane == 0) release_entry(k);
-        break;
-      }
+      if (!qe->valid) break;                     // the last entry: nobody waits for its release
       const int T = qe->T, npt = qe->npt, tail_valid = qe->tail_valid, n = qe->n;
       const int my_rt = qe->rt + (int)rank;         // this CTA's row tile of the pair
       bool row_ok;
@@ -554,19 +565,20 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
             sv[e] = vis ? sv[e] : -INFINITY;
           }
         }
-        float mx8[8];
+        float mq[4] = {sv[0], sv[1], sv[2], sv[3]};
 #pragma unroll
-        for (int a = 0; a < 8; ++a) mx8[a] = sv[a];
-#pragma unroll
-        for (int e = 8; e < 64; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], sv[e]);
-        float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                         fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-        // exchange the half-row maximum with the other half
+        for (int e = 4; e < 64; e += 2) mq[(e >> 1) & 3] = fmax3(mq[(e >> 1) & 3], sv[e], sv[e + 1]);
+        float mx = fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
+        // exchange the half-row maximum with the other half (the row
+        // quarter's two warps meet on their own barrier)
         float* xb = xch + (xt & 1) * 256;
         xb[half * 128 + r] = mx;
         __syncwarp();
-        if (lane == 0) mbar_arrive(XCH(xt & 1));
-        if (!__all_sync(kAll, mbar_wait(XCH(xt & 1), (xt >> 1) & 1, abort_flag, kWaitNs))) { ok = false; break; }
+        if (lane == 0) mbar_arrive(XCH(warp & 3, xt & 1));
+        if (!__all_sync(kAll, mbar_wait(XCH(warp & 3, xt & 1), (xt >> 1) & 1, abort_flag, kWaitNs))) {
+          ok = false;
+          break;
+        }
         ++xt;
         mx = fmaxf(mx, xb[(half ^ 1) * 128 + r]);
         const float m_tile = mx == -INFINITY ? -INFINITY : mx * c2;
@@ -596,19 +608,22 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         }
         if (first) m_ref = m_new;
         const float nm = m_ref == -INFINITY ? 0.f : -m_ref;   // masked keys: 2^-inf = 0
-        float l8[8];
-#pragma unroll
-        for (int a = 0; a < 8; ++a) l8[a] = 0.f;
+        // P = 2^(s c2 - m) in packed pairs (f32x2 products and sums)
+        const uint64_t c2x2 = pk2(c2, c2), nmx2 = pk2(nm, nm);
+        uint64_t l4[4] = {0ull, 0ull, 0ull, 0ull};   // packed (+0, +0)
         uint32_t pk[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const float p0 = ex2(fmaf(sv[2 * e], c2, nm));
-          const float p1 = ex2(fmaf(sv[2 * e + 1], c2, nm));
-          l8[(2 * e) & 7] += p0;
-          l8[(2 * e + 1) & 7] += p1;
-          pk[e] = pack_bf16(p0, p1);
+          const float2 x = up2(ffma2(pk2(sv[2 * e], sv[2 * e + 1]), c2x2, nmx2));
+          const uint64_t y = pk2(ex2(x.x), ex2(x.y));
+          l4[e & 3] = fadd2(l4[e & 3], y);
+          const float2 yf = up2(y);
+          pk[e] = pack_bf16(yf.x, yf.y);
         }
-        l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+        {
+          const float2 la = up2(fadd2(fadd2(l4[0], l4[1]), fadd2(l4[2], l4[3])));
+          l += la.x + la.y;
+        }
         tmem_st_x32(sbuf + half * 32, pk);          // P over the S columns, bf16 pairs
         tc_fence_before();
         __syncwarp();
@@ -632,8 +647,8 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         float* xb = xch + (xt & 1) * 256;
         xb[half * 128 + r] = l;
         __syncwarp();
-        if (lane == 0) mbar_arrive(XCH(xt & 1));
-        epi = __all_sync(kAll, mbar_wait(XCH(xt & 1), (xt >> 1) & 1, abort_flag, kWaitNs));
+        if (lane == 0) mbar_arrive(XCH(warp & 3, xt & 1));
+        epi = __all_sync(kAll, mbar_wait(XCH(warp & 3, xt & 1), (xt >> 1) & 1, abort_flag, kWaitNs));
         ++xt;
         lsum = l + xb[(half ^ 1) * 128 + r];
       }
@@ -685,8 +700,10 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   tc_fence_before();
   __syncthreads();
   // neither CTA leaves while the peer may still write into its shared memory
-  // (multicast copies, commits, queue entries)
-  cluster_sync_all();
+  // (multicast copies are waited by both producers, commits by FIN, remote
+  // queue releases by the scheduler's last wait): an execution-only barrier
+  // suffices
+  cluster_sync_relaxed();
   if (tid == 0 && *abort_flag) set_status(p.status, TV_DEV_TIMEOUT);
   if (warp == 1) {
     tc_fence_after();

@@ -139,6 +139,27 @@ __device__ inline bool seq_rows(const int32_t* offs, int b, int R, int max_nodes
 __device__ __forceinline__ void dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Workspace words that need no zeroing between launches: a word holds a tag
+// (the low 40 bits of the launch's %gridid) above a 24-bit count.  Every
+// user first raises the word to (tag, 0) with an atomic maximum (an earlier
+// launch's word has a smaller tag; memory never written by a launch, with a
+// larger one, is replaced by compare-and-swap) and only then counts with
+// atomic adds.
+__device__ __forceinline__ unsigned long long launch_tag() {
+  unsigned long long g;
+  asm volatile("mov.u64 %0, %%gridid;" : "=l"(g));
+  return (g & ((1ull << 40) - 1)) << 24;
+}
+
+__device__ __forceinline__ void arm_counter(unsigned long long* cnt, unsigned long long tag) {
+  unsigned long long old = atomicMax(cnt, tag);
+  while ((old >> 24) > (tag >> 24)) {               // not an earlier launch's word: replace it
+    const unsigned long long prev = atomicCAS(cnt, old, tag);
+    if (prev == old) break;
+    old = prev;                                     // changed meanwhile (another CTA may have armed it)
+  }
+}
+
 // L2 prefetch of the line holding ptr: no effect on memory ordering, so a
 // kernel may issue it before dep_wait() (it only warms L2 and the TLB for
 // what the kernel reads first, while the previous kernel still runs).
