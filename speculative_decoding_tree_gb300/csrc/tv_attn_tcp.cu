@@ -28,12 +28,15 @@
 // skipped without being handed out.
 //
 //   warp 0      TMA producer: per unit its Q tile, then 32 KB K/V chunks
-//               through a ring of slots in MMA order K(0), K(1), V(0), ...
-//               (sixteen 16-row boxes per chunk on a paged cache).
+//               through a ring of slots in MMA order K(0), K(1), K(2),
+//               V(0), K(3), V(1), ... (sixteen 16-row boxes per chunk on a
+//               paged cache).
 //   warp 1      owns tensor memory; lane 0 issues the MMAs: S(t) = Q K(t)^T
-//               into one of two 128-column buffers, O += P V into one of two
-//               O buffers (alternating by unit, so that a unit's epilogue
-//               can read its O while the next unit accumulates).
+//               into one of three 128-column buffers, two tiles ahead of
+//               O += P(t) V(t) into the one O buffer, so that the softmax
+//               finds S(t + 1) ready when it finishes P(t).  (The unit's
+//               epilogue reads O before the same warps release the next
+//               unit's first P, whose product starts O afresh.)
 //   warp 2      scheduler (lane 0 of the pair's first CTA): takes unit
 //               numbers from the counter, decodes them (lengths, offsets,
 //               chunk bounds) and hands them through a two-entry queue in
@@ -41,8 +44,8 @@
 //   warps 3-10  softmax (two threads per query row, each half of a tile's
 //               keys), then each unit's epilogue, which writes the partial
 //               rows straight from registers.
-// Barrier phases run on across units: slots by a slot counter, the S / P /
-// O buffers by a tile counter, the max / sum exchanges by an exchange
+// Barrier phases run on across units: slots by a slot counter, the S / P
+// buffers and O products by a tile counter, the max / sum exchanges by an exchange
 // counter, per-unit barriers by a unit counter.  Every wait is bounded
 // (1 s); on a timeout the CTA raises TV_DEV_TIMEOUT and every role leaves
 // its loop.
@@ -89,7 +92,7 @@ constexpr int KH = BN / 2;                      // keys of a tile each CTA of th
 
 // barrier numbers
 constexpr int B_FULL = 0, B_EMPTY = NS, B_QFULL = 2 * NS, B_QEMPTY = B_QFULL + 1, B_SFULL = B_QEMPTY + 1,
-              B_PFULL = B_SFULL + 2, B_ODONE = B_PFULL + 2, B_XCH = B_ODONE + 2, B_TAIL = B_XCH + 8,
+              B_PFULL = B_SFULL + 3, B_ODONE = B_PFULL + 3, B_XCH = B_ODONE + 2, B_TAIL = B_XCH + 8,
               B_FIN = B_TAIL + 2, B_UFULL = B_FIN + 1, B_UEMPTY = B_UFULL + kUnitSlots,
               NBARS = B_UEMPTY + kUnitSlots;
 static_assert(NBARS * 8 + 8 <= 384, "barriers overflow the header");
@@ -226,9 +229,11 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     }
     mbar_init(Q_FULL, 1);
     mbar_init(Q_EMPTY, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 3; ++i) {
       mbar_init(S_FULL(i), 1);
       mbar_init(P_FULL(i), kSoftmaxWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(O_DONE(i), 1);
       for (int q = 0; q < 4; ++q) mbar_init(XCH(q, i), 2);   // the row quarter's two warps
     }
@@ -360,18 +365,19 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         return oob_row;                             // out of range: the copy reads zeros
       };
       int pid_a = page_id(0), pid_b = page_id(1), pid_c = page_id(2), pid_d = page_id(3);
-      int row_k = -1, row_v = -1;
-      for (int t = 0; t <= T && ok; ++t) {
-        row_v = row_k;
+      int row_k = -1, row_k1 = -1, row_v = -1;
+      for (int t = 0; t < T + 2 && ok; ++t) {
+        row_v = row_k1;                             // tile t - 2
+        row_k1 = row_k;
         row_k = page_row(pid_a);
         pid_a = pid_b;
         pid_b = pid_c;
         pid_c = pid_d;
         pid_d = page_id(t + 4);
-        for (int kind = 0; kind < 2 && ok; ++kind) {         // 0: K(t), 1: V(t-1)
-          const int tile = kind == 0 ? t : t - 1;
-          if ((kind == 0 && t >= T) || (kind == 1 && t < 1)) continue;
-          if (kind == 1 && !q_loaded && !load_q()) {
+        for (int kind = 0; kind < 2 && ok; ++kind) {         // 0: K(t), 1: V(t-2)
+          const int tile = kind == 0 ? t : t - 2;
+          if ((kind == 0 && t >= T) || (kind == 1 && t < 2)) continue;
+          if ((kind == 1 || t == 1) && !q_loaded && !load_q()) {
             ok = false;
             break;
           }
@@ -460,13 +466,13 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         if (T == 0) break;                          // the last entry: nobody waits for its release
         release_entry(k);                           // only T is needed, and it is read
         k ^= 1;
-        const uint32_t obuf = tmem + 256 + (uint32_t)((uq & 1) * D);
+        const uint32_t obuf = tmem + 384;
         if (!mbar_wait(Q_FULL, uq & 1, abort_flag, kWaitNs)) break;
         tc_fence_after();
-        for (int t = 0; t <= T && ok; ++t) {
+        for (int t = 0; t < T + 2 && ok; ++t) {
           if (t < T) {
             const int tg = tt + t;
-            const uint32_t sbuf = tmem + (uint32_t)((tg & 1) * 128);
+            const uint32_t sbuf = tmem + (uint32_t)((tg % 3) * 128);
             const int slot = j % NS;
             if (!mbar_wait(FULL(slot), (j / NS) & 1, abort_flag, kWaitNs)) { ok = false; break; }
             tc_fence_after();
@@ -478,14 +484,14 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
               mma_ss(sbuf, a, bd, ID_QK, kk > 0 ? 1u : 0u);
             }
             mma_commit_mc(EMPTY(slot), kPair);
-            mma_commit(S_FULL(tg & 1));
+            mma_commit(S_FULL(tg % 3));
             if (t == T - 1) mma_commit(Q_EMPTY);    // the unit's last product that reads Q
             ++j;
           }
-          if (t >= 1) {
-            const int u = t - 1, ug = tt + u;
-            const uint32_t pbuf = tmem + (uint32_t)((ug & 1) * 128);
-            if (!mbar_wait(P_FULL(ug & 1), (ug >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
+          if (t >= 2) {
+            const int u = t - 2, ug = tt + u;
+            const uint32_t pbuf = tmem + (uint32_t)((ug % 3) * 128);
+            if (!mbar_wait(P_FULL(ug % 3), (ug / 3) & 1, abort_flag, kWaitNs)) { ok = false; break; }
             tc_fence_after();
             const int slot = j % NS;
             if (!mbar_wait(FULL(slot), (j / NS) & 1, abort_flag, kWaitNs)) { ok = false; break; }
@@ -538,13 +544,13 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         row_ok = r < p.rows_per_tile && (m0 + r) < n * G;
         anc = row_ok ? p.anc[qe->o0 + (m0 + r) / G] : 0ull;
       }
-      const uint32_t obuf = tmem + lane_base + 256 + (uint32_t)((uq & 1) * D);
+      const uint32_t obuf = tmem + lane_base + 384;
       float m_ref = -INFINITY, l = 0.f;
       for (int t = 0; t < T && ok; ++t) {
         const int tg = tt + t;
-        if (!__all_sync(kAll, mbar_wait(S_FULL(tg & 1), (tg >> 1) & 1, abort_flag, kWaitNs))) { ok = false; break; }
+        if (!__all_sync(kAll, mbar_wait(S_FULL(tg % 3), (tg / 3) & 1, abort_flag, kWaitNs))) { ok = false; break; }
         tc_fence_after();
-        const uint32_t sbuf = tmem + lane_base + (uint32_t)((tg & 1) * 128);
+        const uint32_t sbuf = tmem + lane_base + (uint32_t)((tg % 3) * 128);
         float sv[BN / 2];
         {
           uint32_t rr[64];
@@ -627,7 +633,7 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         tmem_st_x32(sbuf + half * 32, pk);          // P over the S columns, bf16 pairs
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(P_FULL(tg & 1));
+        if (lane == 0) mbar_arrive(P_FULL(tg % 3));
       }
       // epilogue of the unit: the last P V has landed; the two halves' sums
       // are added through the next exchange buffer.  A sequence with one
