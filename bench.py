@@ -2,8 +2,9 @@
 
 One step = one verify round over one batch of synthetic input: tree mask,
 split-KV tree attention + merge, per-node argmax, acceptance walk and the
-accept(k) commit (five launches of this library's kernels), plus a reset of
-prefix_len so that every step verifies the same workload.
+accept(k) commit (five launches of this library's kernels).  Every step
+verifies the same workload: each step of a timed graph has its own copy of
+prefix_len, all reset by one copy at the graph's start.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5] [--impl ours|reference]
 
@@ -359,7 +360,8 @@ def bench_config(spec, w, nsets, per_set, per_big, ws):
         "head_dim": spec.d, "prefix": list(spec.prefix), "tree_rows": int(w.total_rows), "vocab": spec.vocab,
         "paged": spec.paged, "parallelism": "replicas" if ws > 1 else "single",
         "l2": f"inputs rotate over {nsets} copies ({nsets * per_set / 1e6:.0f} MB > 129 MB L2)",
-        "timing": f"CUDA-graph replays of {per_big} whole steps per graph (the remainder one per graph), CUDA events",
+        "timing": (f"CUDA-graph replays of {per_big} whole steps per graph (the remainder one per graph), "
+                   "CUDA events; each step of a graph has its own prefix_len, reset once at the graph's start"),
     }
 
 
@@ -396,10 +398,26 @@ class Harness:
         # so that graph launches do not sit between every two steps; every
         # step in it does all of its work
         self.per_big = self.nsets * max(1, math.ceil(8 / self.nsets))
+        # Each step of the big graph verifies with its own copy of prefix_len
+        # (a 16-byte aligned row of pl_big); one copy at the graph's start
+        # resets them all to the sets' starting lengths, so the commits of
+        # one replay never change the next replay's workload and no reset
+        # sits between two steps.
+        p0 = self.sets[0].p0
+        row = max(4, (p0.numel() + 3) // 4 * 4)
+        self.pl_big = torch.zeros((self.per_big, row), dtype=p0.dtype, device=p0.device)
+        self.p0_big = self.pl_big.clone()
+        for i in range(self.per_big):
+            self.p0_big[i, :p0.numel()] = self.sets[i % self.nsets].p0
         self.big = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.big, stream=cap_stream):
+            self.pl_big.copy_(self.p0_big, non_blocking=True)
             for i in range(self.per_big):
-                self.step(self.sets[i % self.nsets])
+                st = self.sets[i % self.nsets]
+                saved = st.prefix_len
+                st.prefix_len = self.pl_big[i, :p0.numel()]
+                st.step()
+                st.prefix_len = saved
         for i in range(max(warmup, 3)):
             self.graphs[i % self.nsets].replay()
         self.big.replay()
