@@ -129,8 +129,8 @@ tv_attn_tc2_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     mbar_init(TAIL, 1);
     mbar_init(FIN, 1);
     mbar_init(XL, kSoftmaxWarps);
-    // box i: the 4 warps of one half, once per 32-column step it spans
-    for (int i = 0; i < D / 32; ++i) mbar_init(BOX(i), (p.part_bf16 ? 2 : 1) * (kSoftmaxWarps / 2));
+    // box i: the 4 warps of one half, once each
+    for (int i = 0; i < D / 32; ++i) mbar_init(BOX(i), kSoftmaxWarps / 2);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -626,9 +626,16 @@ tv_attn_tc2_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
                              __float_as_uint(__uint_as_float(rr[4 * c4 + 3]) * inv));
           }
         }
+        if (!p.part_bf16) {                        // an fp32 box is one 32-column step
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BOX(half * (D / 64) + q));
+        }
+      }
+      if (p.part_bf16) {                           // a bf16 box is the whole 64-column load
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(BOX(p.part_bf16 ? half * (D / 128) + qq : half * (D / 64) + q));
+        if (lane == 0) mbar_arrive(BOX(half * (D / 128) + qq));
       }
     }
     if (epi && got && rows_here && !direct)
