@@ -28,25 +28,27 @@
 // skipped without being handed out.
 //
 //   warp 0      TMA producer: per unit its Q tile, then 32 KB K/V chunks
-//               through a ring of slots in MMA order K(0), K(1), K(2),
-//               V(0), K(3), V(1), ... (sixteen 16-row boxes per chunk on a
-//               paged cache).
+//               through a ring of slots in MMA order K(0), K(1), V(0),
+//               K(2), V(1), ... (sixteen 16-row boxes per chunk on a paged
+//               cache).
 //   warp 1      owns tensor memory; lane 0 issues the MMAs: S(t) = Q K(t)^T
-//               into one of three 128-column buffers, two tiles ahead of
-//               O += P(t) V(t) into the one O buffer, so that the softmax
-//               finds S(t + 1) ready when it finishes P(t).  (The unit's
-//               epilogue reads O before the same warps release the next
-//               unit's first P, whose product starts O afresh.)
+//               into one of two 128-column buffers, then for each key half h
+//               O_h += P(t)[:, half h] V(t)[half h, :] into that half's own
+//               O accumulator (TMEM columns 256 + 128 h), as soon as that
+//               half's softmax warps have written their P.
 //   warp 2      scheduler (lane 0 of the pair's first CTA): takes unit
 //               numbers from the counter, decodes them (lengths, offsets,
 //               chunk bounds) and hands them through a two-entry queue in
 //               both CTAs' shared memory to the other roles of both.
 //   warps 3-10  softmax (two threads per query row, each half of a tile's
-//               keys), then each unit's epilogue, which writes the partial
-//               rows straight from registers.
+//               keys with its own running maximum, sum and O accumulator, so
+//               the two never wait for each other inside a unit), then each
+//               unit's epilogue: the row's two threads exchange their
+//               maxima and sums once, combine the two accumulators and write
+//               the partial rows straight from registers.
 // Barrier phases run on across units: slots by a slot counter, the S / P
-// buffers and O products by a tile counter, the max / sum exchanges by an exchange
-// counter, per-unit barriers by a unit counter.  Every wait is bounded
+// buffers and O products by a tile counter, the epilogue's exchanges by an
+// exchange counter, per-unit barriers by a unit counter.  Every wait is bounded
 // (1 s); on a timeout the CTA raises TV_DEV_TIMEOUT and every role leaves
 // its loop.
 //
@@ -92,7 +94,7 @@ constexpr int KH = BN / 2;                      // keys of a tile each CTA of th
 
 // barrier numbers
 constexpr int B_FULL = 0, B_EMPTY = NS, B_QFULL = 2 * NS, B_QEMPTY = B_QFULL + 1, B_SFULL = B_QEMPTY + 1,
-              B_PFULL = B_SFULL + 3, B_ODONE = B_PFULL + 3, B_XCH = B_ODONE + 2, B_TAIL = B_XCH + 8,
+              B_PFULL = B_SFULL + 2, B_ODONE = B_PFULL + 4, B_XCH = B_ODONE + 4, B_TAIL = B_XCH + 8,
               B_FIN = B_TAIL + 2, B_UFULL = B_FIN + 1, B_UEMPTY = B_UFULL + kUnitSlots,
               NBARS = B_UEMPTY + kUnitSlots;
 static_assert(NBARS * 8 + 8 <= 384, "barriers overflow the header");
@@ -209,8 +211,8 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   const uint32_t Q_FULL = bar(B_QFULL), Q_EMPTY = bar(B_QEMPTY), FIN = bar(B_FIN);
   auto TAIL = [&](int i) { return bar(B_TAIL + i); };
   auto S_FULL = [&](int i) { return bar(B_SFULL + i); };
-  auto P_FULL = [&](int i) { return bar(B_PFULL + i); };
-  auto O_DONE = [&](int i) { return bar(B_ODONE + i); };
+  auto P_FULL = [&](int h, int i) { return bar(B_PFULL + 2 * h + i); };   // key half h, parity i
+  auto O_DONE = [&](int h, int i) { return bar(B_ODONE + 2 * h + i); };
   auto XCH = [&](int q, int i) { return bar(B_XCH + 2 * q + i); };   // row quarter q, parity i
   auto UFULL = [&](int i) { return bar(B_UFULL + i); };
   auto UEMPTY = [&](int i) { return bar(B_UEMPTY + i); };
@@ -229,12 +231,12 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     }
     mbar_init(Q_FULL, 1);
     mbar_init(Q_EMPTY, 1);
-    for (int i = 0; i < 3; ++i) {
-      mbar_init(S_FULL(i), 1);
-      mbar_init(P_FULL(i), kSoftmaxWarps);
-    }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(O_DONE(i), 1);
+      mbar_init(S_FULL(i), 1);
+      for (int h = 0; h < 2; ++h) {
+        mbar_init(P_FULL(h, i), kSoftmaxWarps / 2);   // the warps of key half h
+        mbar_init(O_DONE(h, i), 1);
+      }
       for (int q = 0; q < 4; ++q) mbar_init(XCH(q, i), 2);   // the row quarter's two warps
     }
     mbar_init(TAIL(0), 1);
@@ -365,19 +367,18 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         return oob_row;                             // out of range: the copy reads zeros
       };
       int pid_a = page_id(0), pid_b = page_id(1), pid_c = page_id(2), pid_d = page_id(3);
-      int row_k = -1, row_k1 = -1, row_v = -1;
-      for (int t = 0; t < T + 2 && ok; ++t) {
-        row_v = row_k1;                             // tile t - 2
-        row_k1 = row_k;
+      int row_k = -1, row_v = -1;
+      for (int t = 0; t <= T && ok; ++t) {
+        row_v = row_k;                              // tile t - 1
         row_k = page_row(pid_a);
         pid_a = pid_b;
         pid_b = pid_c;
         pid_c = pid_d;
         pid_d = page_id(t + 4);
-        for (int kind = 0; kind < 2 && ok; ++kind) {         // 0: K(t), 1: V(t-2)
-          const int tile = kind == 0 ? t : t - 2;
-          if ((kind == 0 && t >= T) || (kind == 1 && t < 2)) continue;
-          if ((kind == 1 || t == 1) && !q_loaded && !load_q()) {
+        for (int kind = 0; kind < 2 && ok; ++kind) {         // 0: K(t), 1: V(t-1)
+          const int tile = kind == 0 ? t : t - 1;
+          if ((kind == 0 && t >= T) || (kind == 1 && t < 1)) continue;
+          if (kind == 1 && !q_loaded && !load_q()) {
             ok = false;
             break;
           }
@@ -466,13 +467,12 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         if (T == 0) break;                          // the last entry: nobody waits for its release
         release_entry(k);                           // only T is needed, and it is read
         k ^= 1;
-        const uint32_t obuf = tmem + 384;
         if (!mbar_wait(Q_FULL, uq & 1, abort_flag, kWaitNs)) break;
         tc_fence_after();
-        for (int t = 0; t < T + 2 && ok; ++t) {
+        for (int t = 0; t <= T && ok; ++t) {
           if (t < T) {
             const int tg = tt + t;
-            const uint32_t sbuf = tmem + (uint32_t)((tg % 3) * 128);
+            const uint32_t sbuf = tmem + (uint32_t)((tg & 1) * 128);
             const int slot = j % NS;
             if (!mbar_wait(FULL(slot), (j / NS) & 1, abort_flag, kWaitNs)) { ok = false; break; }
             tc_fence_after();
@@ -484,26 +484,33 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
               mma_ss(sbuf, a, bd, ID_QK, kk > 0 ? 1u : 0u);
             }
             mma_commit_mc(EMPTY(slot), kPair);
-            mma_commit(S_FULL(tg % 3));
+            mma_commit(S_FULL(tg & 1));
             if (t == T - 1) mma_commit(Q_EMPTY);    // the unit's last product that reads Q
             ++j;
           }
-          if (t >= 2) {
-            const int u = t - 2, ug = tt + u;
-            const uint32_t pbuf = tmem + (uint32_t)((ug % 3) * 128);
-            if (!mbar_wait(P_FULL(ug % 3), (ug / 3) & 1, abort_flag, kWaitNs)) { ok = false; break; }
-            tc_fence_after();
+          if (t >= 1) {
+            // O_h += P(:, keys of half h) V(keys of half h, :): each key half
+            // of the softmax keeps its own accumulator, maximum and sum, so
+            // the halves never wait for each other inside a unit
+            const int u = t - 1, ug = tt + u;
+            const uint32_t pbuf = tmem + (uint32_t)((ug & 1) * 128);
             const int slot = j % NS;
             if (!mbar_wait(FULL(slot), (j / NS) & 1, abort_flag, kWaitNs)) { ok = false; break; }
             tc_fence_after();
             const uint32_t vaddr = ring_addr + slot * SLOT_BYTES;
+            for (int h = 0; h < 2 && ok; ++h) {
+              if (!mbar_wait(P_FULL(h, ug & 1), (ug >> 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
+              tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk) {  // 16 keys per step
-              const uint64_t bd = smem_desc(vaddr + kk * (16 * 128), BOX_BYTES, 1024, 2);
-              mma_ts(obuf, pbuf + kk * 8, bd, ID_PV, (u > 0 || kk > 0) ? 1u : 0u);
+              for (int kq = 0; kq < BN / 32; ++kq) {  // 16 keys per step, 4 steps per half
+                const int kk = h * (BN / 32) + kq;
+                const uint64_t bd = smem_desc(vaddr + kk * (16 * 128), BOX_BYTES, 1024, 2);
+                mma_ts(tmem + 256 + (uint32_t)(h * D), pbuf + kk * 8, bd, ID_PV, (u > 0 || kq > 0) ? 1u : 0u);
+              }
+              mma_commit(O_DONE(h, ug & 1));
             }
+            if (!ok) break;
             mma_commit_mc(EMPTY(slot), kPair);
-            mma_commit(O_DONE(ug & 1));
             ++j;
           }
         }
@@ -518,16 +525,30 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     }
   } else if (warp >= kFirstSoftmaxWarp) {
     // ============================================================ softmax
-    // Two warpgroups: `half` 0 takes keys 0-63 of every tile (and O columns
-    // 0-63), half 1 keys 64-127 (and columns 64-127); the two threads of a
-    // row share its running maximum (and at the end its sum) through `xch`.
+    // Two warpgroups: `half` 0 takes keys 0-63 of every tile, half 1 keys
+    // 64-127.  Each half keeps its own running maximum, sum and O
+    // accumulator (TMEM columns 256 + 128 half), so the two threads of a row
+    // meet only at the unit's end, where their (maximum, sum) pairs are
+    // exchanged through `xch` and the two accumulators combined.
     const int half = (warp - kFirstSoftmaxWarp) >> 2;
     const int r = (warp & 3) * 32 + lane;           // row in the tile == TMEM lane (warp % 4 picks the quarter)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const float c2 = p.scale_log2;
     const int kofs = half * (BN / 2);
+    const uint32_t obuf = tmem + lane_base + 256 + (uint32_t)(half * D);   // this half's O rows
     int tt = 0, xt = 0, uq = 0, k = 0;
     bool ok = true;
+    // the row quarter's two warps exchange one float per row through xch
+    auto exchange = [&](float mine, float& theirs) -> bool {
+      float* xb = xch + (xt & 1) * 256;
+      xb[half * 128 + r] = mine;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(XCH(warp & 3, xt & 1));
+      const bool in = __all_sync(kAll, mbar_wait(XCH(warp & 3, xt & 1), (xt >> 1) & 1, abort_flag, kWaitNs));
+      ++xt;
+      theirs = xb[(half ^ 1) * 128 + r];
+      return in;
+    };
     while (ok) {
       if (!__all_sync(kAll, mbar_wait_cluster(UFULL(k), (uq / kUnitSlots) & 1, abort_flag, kWaitNs))) break;
       // the entry stays valid until this warp arrives on UEMPTY at the end of
@@ -544,13 +565,12 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         row_ok = r < p.rows_per_tile && (m0 + r) < n * G;
         anc = row_ok ? p.anc[qe->o0 + (m0 + r) / G] : 0ull;
       }
-      const uint32_t obuf = tmem + lane_base + 384;
       float m_ref = -INFINITY, l = 0.f;
       for (int t = 0; t < T && ok; ++t) {
         const int tg = tt + t;
-        if (!__all_sync(kAll, mbar_wait(S_FULL(tg % 3), (tg / 3) & 1, abort_flag, kWaitNs))) { ok = false; break; }
+        if (!__all_sync(kAll, mbar_wait(S_FULL(tg & 1), (tg >> 1) & 1, abort_flag, kWaitNs))) { ok = false; break; }
         tc_fence_after();
-        const uint32_t sbuf = tmem + lane_base + (uint32_t)((tg % 3) * 128);
+        const uint32_t sbuf = tmem + lane_base + (uint32_t)((tg & 1) * 128);
         float sv[BN / 2];
         {
           uint32_t rr[64];
@@ -574,39 +594,28 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         float mq[4] = {sv[0], sv[1], sv[2], sv[3]};
 #pragma unroll
         for (int e = 4; e < 64; e += 2) mq[(e >> 1) & 3] = fmax3(mq[(e >> 1) & 3], sv[e], sv[e + 1]);
-        float mx = fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
-        // exchange the half-row maximum with the other half (the row
-        // quarter's two warps meet on their own barrier)
-        float* xb = xch + (xt & 1) * 256;
-        xb[half * 128 + r] = mx;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(XCH(warp & 3, xt & 1));
-        if (!__all_sync(kAll, mbar_wait(XCH(warp & 3, xt & 1), (xt >> 1) & 1, abort_flag, kWaitNs))) {
-          ok = false;
-          break;
-        }
-        ++xt;
-        mx = fmaxf(mx, xb[(half ^ 1) * 128 + r]);
+        const float mx = fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
         const float m_tile = mx == -INFINITY ? -INFINITY : mx * c2;
         const float m_new = fmaxf(m_ref, m_tile);
         const bool first = (m_ref == -INFINITY);
         const bool need = !first && (m_new > m_ref + kRescaleThreshold);
         if (__any_sync(kAll, need)) {
-          // the O rows must hold P(t-1) V(t-1) before they are rescaled (t >= 1 here)
+          // this half's O rows must hold P(t-1) V(t-1) before they are rescaled (t >= 1 here)
           const int ug = tg - 1;
-          if (!__all_sync(kAll, mbar_wait(O_DONE(ug & 1), (ug >> 1) & 1, abort_flag, kWaitNs))) { ok = false; break; }
+          if (!__all_sync(kAll, mbar_wait(O_DONE(half, ug & 1), (ug >> 1) & 1, abort_flag, kWaitNs))) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const float alpha = need ? ex2(m_ref - m_new) : 1.f;
-          uint32_t rr[32];
-          const uint32_t oa = obuf + half * (D / 2);
-          tmem_ld_x32(oa, rr);
+#pragma unroll 1
+          for (int c = 0; c < D; c += 32) {
+            uint32_t rr[32];
+            tmem_ld_x32(obuf + c, rr);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
-          tmem_st_x32(oa, rr);
-          tmem_ld_x32(oa + 32, rr);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
-          tmem_st_x32(oa + 32, rr);
+            for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
+            tmem_st_x32(obuf + c, rr);
+          }
           if (need) {
             l *= alpha;
             m_ref = m_new;
@@ -633,66 +642,67 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         tmem_st_x32(sbuf + half * 32, pk);          // P over the S columns, bf16 pairs
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(P_FULL(tg % 3));
+        if (lane == 0) mbar_arrive(P_FULL(half, tg & 1));
       }
-      // epilogue of the unit: the last P V has landed; the two halves' sums
-      // are added through the next exchange buffer.  A sequence with one
-      // chunk writes its normalised rows directly; otherwise the partial
-      // O_s / l_s (bf16) is staged in 128-byte swizzled boxes (box = half)
-      // once the store warp has released the previous unit's staging, and
-      // each box's barrier is arrived in every path.
+      // Epilogue of the unit: both halves' last products have landed; the
+      // two threads of a row exchange their maxima and sums, and each writes
+      // its 64 columns of (a0 O_0 + a1 O_1) / L with a_h = 2^(m_h - M),
+      // M = max(m_0, m_1), L = a0 l_0 + a1 l_1 -- the normalised rows for a
+      // sequence with one chunk, else the partial with (M, L) for the merge.
       const int ul = tt + T - 1;
       const bool direct = p.out != nullptr && qe->nch == 1;
       // the pair's second tile may lie past the tree's rows (or past the
       // last row tile): it computes on zeros and writes nothing
       const bool tile_live = my_rt < p.row_tiles && my_rt * p.rows_per_tile < qe->n * G;
-      bool epi = ok && __all_sync(kAll, mbar_wait(O_DONE(ul & 1), (ul >> 1) & 1, abort_flag, kWaitNs));
-      float lsum = 0.f;
+      bool epi = ok && __all_sync(kAll, mbar_wait(O_DONE(0, ul & 1), (ul >> 1) & 1, abort_flag, kWaitNs) &&
+                                            mbar_wait(O_DONE(1, ul & 1), (ul >> 1) & 1, abort_flag, kWaitNs));
+      float m_p = -INFINITY, l_p = 0.f;
       if (epi) {
         tc_fence_after();
-        float* xb = xch + (xt & 1) * 256;
-        xb[half * 128 + r] = l;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(XCH(warp & 3, xt & 1));
-        epi = __all_sync(kAll, mbar_wait(XCH(warp & 3, xt & 1), (xt >> 1) & 1, abort_flag, kWaitNs));
-        ++xt;
-        lsum = l + xb[(half ^ 1) * 128 + r];
+        epi = exchange(m_ref, m_p);
+        epi = exchange(l, l_p) && epi;
       }
-      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-      uint32_t rv[64];
-      if (epi) tmem_ld_x64(obuf + half * (D / 2), rv);
-      if (epi && direct && row_ok) {
+      const float M = fmaxf(m_ref, m_p);
+      const float a_self = m_ref == -INFINITY ? 0.f : ex2(m_ref - M);
+      const float a_peer = m_p == -INFINITY ? 0.f : ex2(m_p - M);
+      const float L = l * a_self + l_p * a_peer;
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      const float w0 = (half == 0 ? a_self : a_peer) * inv, w1 = (half == 0 ? a_peer : a_self) * inv;
+      __nv_bfloat16* dst = nullptr;
+      if (direct && row_ok) {
         const int m = my_rt * p.rows_per_tile + r;   // query row of the KV head: node m / G, head g G + m % G
-        const int64_t e0 = ((int64_t)(qe->o0 + m / G) * p.Hq + qe->g * G + m % G) * D + half * (D / 2);
-        uint4* ob = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + e0);
+        dst = reinterpret_cast<__nv_bfloat16*>(p.out) + ((int64_t)(qe->o0 + m / G) * p.Hq + qe->g * G + m % G) * D;
+      } else if (!direct && tile_live) {
+        dst = reinterpret_cast<__nv_bfloat16*>(p.o_part) +
+              partial_slot(qe->s, qe->b, qe->g, my_rt, r, p.Hkv, p.row_tiles, BM, p.splits) * D;
+      }
+#pragma unroll 1
+      for (int c = 0; c < D / 2 && epi; c += 32) {   // this thread's 64 columns, 32 at a time
+        const int col = half * (D / 2) + c;
+        uint32_t r0[32], r1[32];
+        tmem_ld_x32(tmem + lane_base + 256 + col, r0);
+        tmem_ld_x32(tmem + lane_base + 256 + D + col, r1);
+        if (dst != nullptr) {
+          uint4* ob = reinterpret_cast<uint4*>(dst + col);
 #pragma unroll
-        for (int e8 = 0; e8 < 8; ++e8) {
-          uint4 w4;
-          w4.x = pack_bf16(__uint_as_float(rv[8 * e8 + 0]) * inv, __uint_as_float(rv[8 * e8 + 1]) * inv);
-          w4.y = pack_bf16(__uint_as_float(rv[8 * e8 + 2]) * inv, __uint_as_float(rv[8 * e8 + 3]) * inv);
-          w4.z = pack_bf16(__uint_as_float(rv[8 * e8 + 4]) * inv, __uint_as_float(rv[8 * e8 + 5]) * inv);
-          w4.w = pack_bf16(__uint_as_float(rv[8 * e8 + 6]) * inv, __uint_as_float(rv[8 * e8 + 7]) * inv);
-          ob[e8] = w4;
-        }
-      } else if (epi && !direct && tile_live) {
-        // this row's half of the partial, straight to its slot
-        uint4* ob = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o_part) +
-                                             partial_slot(qe->s, qe->b, qe->g, my_rt, r, p.Hkv, p.row_tiles, BM,
-                                                          p.splits) * D + half * (D / 2));
+          for (int e8 = 0; e8 < 4; ++e8) {
+            float v[8];
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
-          uint4 w4;
-          w4.x = pack_bf16(__uint_as_float(rv[8 * c8 + 0]) * inv, __uint_as_float(rv[8 * c8 + 1]) * inv);
-          w4.y = pack_bf16(__uint_as_float(rv[8 * c8 + 2]) * inv, __uint_as_float(rv[8 * c8 + 3]) * inv);
-          w4.z = pack_bf16(__uint_as_float(rv[8 * c8 + 4]) * inv, __uint_as_float(rv[8 * c8 + 5]) * inv);
-          w4.w = pack_bf16(__uint_as_float(rv[8 * c8 + 6]) * inv, __uint_as_float(rv[8 * c8 + 7]) * inv);
-          ob[c8] = w4;
+            for (int q = 0; q < 8; ++q)
+              v[q] = __uint_as_float(r0[8 * e8 + q]) * w0 + __uint_as_float(r1[8 * e8 + q]) * w1;
+            uint4 w4;
+            w4.x = pack_bf16(v[0], v[1]);
+            w4.y = pack_bf16(v[2], v[3]);
+            w4.z = pack_bf16(v[4], v[5]);
+            w4.w = pack_bf16(v[6], v[7]);
+            ob[e8] = w4;
+          }
         }
       }
       tc_fence_before();
-      if (epi && !direct && tile_live)
+      if (epi && !direct && tile_live && half == 0)
         p.ml_part[partial_slot(qe->s, qe->b, qe->g, my_rt, r, p.Hkv, p.row_tiles, BM, p.splits)] =
-            make_float2(row_ok ? m_ref : -INFINITY, row_ok ? lsum : 0.f);
+            make_float2(row_ok ? M : -INFINITY, row_ok ? L : 0.f);
       __syncwarp();
       if (lane == 0) release_entry(k);             // done with the queue entry
       k ^= 1;
