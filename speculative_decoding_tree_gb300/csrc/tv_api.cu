@@ -121,11 +121,13 @@ int make_plan(const tv_desc* d, Plan* p) {
     while (c <= tiles && num_chunks(L, (int)(c * key_tile), tree_tile) > want) ++c;
     chunk = c * key_tile;
   } else {
-    // ragged batch: fixed 2048-key chunks (16 key tiles of 128) so that the
-    // block scheduler balances sequences of different lengths (on the
-    // batched workload 512 / 1024 / 2048 / 4096 keys gave a split pass of
-    // 174 / 137 / 130 / 131 us)
-    chunk = align_up(2048, key_tile);
+    // ragged batch: fixed 1920-key chunks (15 key tiles of 128), so that the
+    // units balance sequences of different lengths.  On the batched
+    // workload's persistent kernel, summed over three seeds of its prefixes
+    // and trees, the call took 348.8 / 343.1 / 341.0 / 345.0 us with 1664 /
+    // 1792 / 1920 / 2048-key chunks; on one seed 1024 and 4096 keys gave
+    // 128.9 and 132.2 us against 120.3 at 2048)
+    chunk = align_up(1920, key_tile);
   }
   if (chunk > (int64_t)1 << 30) return TV_ERR_OVERFLOW;
   int splits = num_chunks(L, (int)chunk, tree_tile);

@@ -80,16 +80,19 @@ def test_grid_limits_refused_on_the_host(L):
     big_batch = _desc(batch=70000, total_rows=70000, max_nodes=1, capacity=64, max_prefix=64)
     assert L.tv_workspace_size(ctypes.byref(big_batch), 0, ctypes.byref(n)) == -6
     assert L.tree_verify_attn(ctypes.byref(big_batch), *([fake] * 10), fake, 1 << 30, fake, None) == -6
-    # 64 KV heads x 1100 chunks of 2048 keys on the one-CTA tensor-core kernel
-    # (16 rows per KV head; an fp32 output keeps the batch off the persistent kernel)
+    # 64 KV heads x 1100 chunks of the batch chunk (1920 keys) on the one-CTA
+    # tensor-core kernel (16 rows per KV head; an fp32 output keeps the batch
+    # off the persistent kernel): 64 x 1100 (KV head, split) pairs exceed the
+    # grid's y limit, 64 x 1000 do not
     many_splits = _desc(batch=2, num_q_heads=256, num_kv_heads=64, head_dim=128, max_nodes=4, total_rows=8,
-                        capacity=2048 * 1100, max_prefix=2048 * 1100, out_f32=1)
+                        capacity=1920 * 1100, max_prefix=1920 * 1100, out_f32=1)
     assert tv.tv_attn_plan(_desc(batch=2, num_q_heads=256, num_kv_heads=64, head_dim=128, max_nodes=4,
-                                 total_rows=8, capacity=2048 * 1000, max_prefix=2048 * 1000,
+                                 total_rows=8, capacity=1920 * 1000, max_prefix=1920 * 1000,
                                  out_f32=1))["kernel"] == 1
     assert L.tv_workspace_size(ctypes.byref(many_splits), 0, ctypes.byref(n)) == -6
     ok_splits = _desc(batch=2, num_q_heads=256, num_kv_heads=64, head_dim=128, max_nodes=4, total_rows=8,
-                      capacity=2048 * 1000, max_prefix=2048 * 1000, out_f32=1)
+                      capacity=1920 * 1000, max_prefix=1920 * 1000, out_f32=1)
+    assert tv.tv_attn_plan(ok_splits)["chunk"] == 1920 and tv.tv_attn_plan(ok_splits)["num_splits"] == 1000
     assert L.tv_workspace_size(ctypes.byref(ok_splits), 0, ctypes.byref(n)) == 0
     # the persistent batch kernel (bf16 output) counts its work units in 24 bits
     units_ok = _desc(batch=2, num_q_heads=256, num_kv_heads=64, head_dim=128, max_nodes=4, total_rows=8,
