@@ -13,10 +13,10 @@
 //
 // The two CTAs of a pair read the same K/V tiles, so each loads half of
 // every tile (its pages, or its 64 keys) with TMA multicast into both CTAs'
-// shared memory.  On a paged cache a 128-key tile is sixteen 16-row boxes
-// and the TMA unit's cost per box sets this path's pace: the pair halves the
-// boxes each SM issues.  A tree whose rows fill one tile leaves the second
-// CTA's rows empty; it still takes its half of the loads.
+// shared memory: L2 serves each K/V byte once per unit, and each SM issues
+// half of a paged tile's sixteen 16-row boxes.  A tree whose rows fill one
+// tile leaves the second CTA's rows empty; it still takes its half of the
+// loads.
 //
 // In a batch the sequences have different prefix lengths and tree sizes, so
 // a grid of one CTA per unit runs in uneven waves and pays the CTA's setup
@@ -25,7 +25,7 @@
 // counter in the workspace until none is left; units are numbered
 // chunk-major (every sequence's first chunk first), so the long full chunks
 // go out before the short last ones.  Units with no rows or no keys are
-// skipped without being handed out.
+// skipped by the scheduler, never queued.
 //
 //   warp 0      TMA producer: per unit its Q tile, then 32 KB K/V chunks
 //               through a ring of slots in MMA order K(0), K(1), V(0),
