@@ -13,9 +13,12 @@
 
 #include "tv_internal.cuh"
 #include "tv_accept.cuh"
+#include "tc_ptx.cuh"
 
 namespace tv {
 namespace {
+
+using namespace tc;
 
 // ----------------------------------------------------------------- A0
 
@@ -358,24 +361,36 @@ __global__ __launch_bounds__(256) void sample_partial_kernel(const AcceptParams 
 
 // ----------------------------------------------------------------- A4 + A5
 
-// The walk and commit of one sequence, run by one block of 256 threads:
-// the block finishes the argmax of every node from its chunk partials (four
-// threads per node) or takes the given one; warp 0 builds ancestors and
-// depths and walks (lane i owns nodes i and i + 32; ballots and shuffles, no
-// shared atomics); then the block copies the accepted K/V rows into the
-// cache, and thread 0 advances prefix_len.
+// The walk and commit of one sequence, run by a cluster of C blocks of 256
+// threads, C = min(8, 2 Hkv): the rows to commit fall into 2 Hkv sets (K or
+// V, KV head), and block x of the cluster copies sets x, x + C, ...  Every
+// block finishes the argmax of every node from its chunk partials (four
+// threads per node) or takes the given one, and walks (warp 0: lane i owns
+// nodes i and i + 32; ballots and shuffles, no shared atomics); the blocks
+// reach the same path from the same inputs, and block 0 alone writes the
+// outputs.  Where a block's sets fit in shared memory, it stages the
+// sequence's tree rows of its sets there by bulk copies while the pass
+// kernel still runs, so that after the walk the commit only stores.  Block 0
+// advances prefix_len behind a cluster barrier that each block arrives on
+// once it has read the old value.
 constexpr int kCommitPages = kMaxNodes / kPageSize + 1;   // pages the k + 1 <= 64 rows can touch
-constexpr int kCommitRows = 256;                            // rows per pass of the commit copy
 constexpr int kWalkThreads = 256;
+constexpr uint64_t kWalkWaitNs = 1000000000ull;           // bound on the staging copies' wait
 
 struct WalkSmem {
   int par[kMaxNodes], draft[kMaxNodes], am[kMaxNodes], path[kMaxNodes];
   uint64_t anc[kMaxNodes];
   int pid[kCommitPages];
-  const uint4* src[kCommitRows];
-  uint4* dst[kCommitRows];
-  int k, ok;
+  int k, ok, abort_flag;
+  alignas(8) uint64_t staged;                        // mbarrier: the staging copies have landed
 };
+
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 
 // what warp 0 keeps of the tree (lane i: nodes i and i + 32)
 struct WalkRegs {
@@ -461,23 +476,107 @@ __device__ void walk_invalid(const AcceptParams& p, int b) {
   if (tid == 0) p.accept_len[b] = -1;
 }
 
+// Thread 0 starts the bulk copies of this block's sets of sequence b: set j
+// = (K or V, KV head g) holds the sequence's n tree rows contiguously (rows
+// o0 .. o0 + n - 1 of head g), staged at slot m = (j - x) / C, max_nodes rows
+// per slot.  Addresses and sizes are multiples of 16 bytes (the host checks
+// the buffers' alignment; a row is d * esize bytes, a multiple of 16).
+__device__ void walk_stage_rows(const AcceptParams& p, WalkSmem& s, char* stage, int o0, int n) {
+  if (threadIdx.x != 0) return;
+  const int C = (int)gridDim.x;
+  const int64_t row_bytes = (int64_t)p.d * p.esize;
+  const uint32_t bar = smem_u32(&s.staged);
+  uint32_t total = 0;
+  for (int j = blockIdx.x; j < 2 * p.Hkv; j += C) total += (uint32_t)(n * row_bytes);
+  mbar_expect_tx(bar, total);
+  for (int j = blockIdx.x, m = 0; j < 2 * p.Hkv; j += C, ++m) {
+    const int kind = j / p.Hkv, g = j - kind * p.Hkv;
+    const char* src = reinterpret_cast<const char*>(kind ? p.v_tree : p.k_tree) + ((int64_t)g * p.R + o0) * row_bytes;
+    if (n > 0) bulk_load(smem_u32(stage + (int64_t)m * p.max_nodes * row_bytes), src, (uint32_t)(n * row_bytes), bar);
+  }
+}
+
+// The commit: rows t = 0 .. k of this block's sets, from the staged rows or
+// (sets too large to stage) from the tree buffers, into cache positions
+// P + t.  16-byte units (unit u: row u / units_row), up to 8 loads in flight
+// per thread, all issued before the stores.
+__device__ void walk_commit_rows(const AcceptParams& p, int b, const WalkSmem& s, const char* stage, int o0, int P,
+                                 int k) {
+  const int C = (int)gridDim.x, tid = threadIdx.x;
+  const int64_t row_bytes = (int64_t)p.d * p.esize;
+  const int units_row = (int)(row_bytes / 16);      // a power of two (16 .. 128)
+  const int ushift = __ffs(units_row) - 1;
+  const int sets = (2 * p.Hkv - (int)blockIdx.x + C - 1) / C;
+  const int total = sets * (k + 1) * units_row;
+  constexpr int U = 8;
+  for (int base = 0; base < total; base += U * (int)blockDim.x) {
+    uint4 v[U];
+    uint4* dst[U];
+#pragma unroll
+    for (int q = 0; q < U; ++q) {
+      const int u = base + q * (int)blockDim.x + tid;
+      dst[q] = nullptr;
+      if (u < total) {
+        const int rr = u >> ushift, w = u & (units_row - 1);
+        const int m = rr / (k + 1), t = rr - m * (k + 1);
+        const int j = (int)blockIdx.x + m * C, kind = j / p.Hkv, g = j - kind * p.Hkv;
+        const int node = s.path[t];
+        const int64_t pos = (int64_t)P + t;
+        int64_t drow;
+        if (p.paged) {
+          const int pid = s.pid[(P + t) / kPageSize - P / kPageSize];
+          drow = ((int64_t)pid * p.Hkv + g) * kPageSize + pos % kPageSize;
+        } else {
+          drow = ((int64_t)b * p.Hkv + g) * p.capacity + pos;
+        }
+        if (stage) {
+          v[q] = reinterpret_cast<const uint4*>(stage + ((int64_t)m * p.max_nodes + node) * row_bytes)[w];
+        } else {
+          const char* src = reinterpret_cast<const char*>(kind ? p.v_tree : p.k_tree) +
+                            ((int64_t)g * p.R + o0 + node) * row_bytes;
+          v[q] = __ldcg(reinterpret_cast<const uint4*>(src) + w);
+        }
+        dst[q] = reinterpret_cast<uint4*>(reinterpret_cast<char*>(kind ? p.v_cache : p.k_cache) + drow * row_bytes) + w;
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < U; ++q)
+      if (dst[q]) *dst[q] = v[q];
+  }
+}
+
 // Part 2: each node's argmax (the caller's, or finished from the chunk
-// partials, which other blocks of the same grid may have written: read
-// through L2), the walk, the outputs, the commit and the new prefix length.
-__device__ void walk_finish(const AcceptParams& p, int b, WalkSmem& s, const WalkRegs& wr, int o0, int n, int P) {
+// partials, which other blocks of the pass grid wrote: read through L2), the
+// walk, the outputs (block 0) and the commit of this block's sets.
+__device__ void walk_finish(const AcceptParams& p, int b, WalkSmem& s, const WalkRegs& wr, const char* stage, int o0,
+                            int n, int P) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool lead = blockIdx.x == 0;
   if (p.given_argmax) {
     if (tid < n) s.am[tid] = p.argmax[o0 + tid];
   } else {
     // argmax of node tid / 4 from chunks c = tid % 4, + 4, ...; max value,
-    // smallest index (better() is order-free), NaN never enters
+    // smallest index (better() is order-free), NaN never enters.  All of a
+    // thread's partials are loaded before the first comparison: one L2
+    // round instead of one per chunk.
+    constexpr int kPer = kMaxVChunks / 4;
+    static_assert(kMaxVChunks % 4 == 0, "four threads per node share the chunks");
     const int vc = p.vchunks;
     const int i = tid >> 2;
+    const bool live = i < n;
+    const int64_t pbase = (int64_t)(o0 + (live ? i : 0)) * vc;
+    float pv[kPer];
+    int pi[kPer];
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int c = (tid & 3) + 4 * q;
+      const bool use = live && c < vc;
+      pv[q] = use ? __ldcg(p.am_val + pbase + c) : 0.f;
+      pi[q] = use ? __ldcg(p.am_idx + pbase + c) : -1;
+    }
     Best bst{-FLT_MAX, -1};
-    if (i < n)
-      for (int c = tid & 3; c < vc; c += 4)
-        bst = better(bst, Best{__ldcg(p.am_val + (int64_t)(o0 + i) * vc + c),
-                               __ldcg(p.am_idx + (int64_t)(o0 + i) * vc + c)});
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) bst = better(bst, Best{pv[q], pi[q]});
 #pragma unroll
     for (int off = 1; off < 4; off <<= 1) {
       Best o;
@@ -488,7 +587,7 @@ __device__ void walk_finish(const AcceptParams& p, int b, WalkSmem& s, const Wal
     if (i < n && (tid & 3) == 0) {
       const int am = bst.i < 0 ? 0 : bst.i;
       s.am[i] = am;
-      p.argmax[o0 + i] = am;
+      if (lead) p.argmax[o0 + i] = am;
     }
   }
   __syncthreads();
@@ -505,7 +604,7 @@ __device__ void walk_finish(const AcceptParams& p, int b, WalkSmem& s, const Wal
         mt[hlf] = (i == 0) || (wr.tree_ok[hlf] && s.draft[i] == s.am[s.par[i]]);
       }
     }
-    if (__any_sync(all, bad) && lane == 0) set_status(p.status, TV_DEV_BAD_TREE);
+    if (__any_sync(all, bad) && lane == 0 && lead) set_status(p.status, TV_DEV_BAD_TREE);
     const uint64_t match = (uint64_t)__ballot_sync(all, mt[0]) | ((uint64_t)__ballot_sync(all, mt[1]) << 32);
     // reachable = every node on the root path matches; best = deepest, then
     // smallest index
@@ -528,7 +627,7 @@ __device__ void walk_finish(const AcceptParams& p, int b, WalkSmem& s, const Wal
 #pragma unroll
     for (int hlf = 0; hlf < 2; ++hlf) {
       const int t = lane + 32 * hlf;
-      if (t < p.max_nodes) {
+      if (t < p.max_nodes && lead) {
         const int64_t o = (int64_t)b * p.max_nodes + t;
         p.path[o] = t <= k ? s.path[t] : -1;
         p.tokens[o] = t < k ? s.draft[s.path[t + 1]] : (t == k ? s.am[end] : -1);
@@ -538,10 +637,10 @@ __device__ void walk_finish(const AcceptParams& p, int b, WalkSmem& s, const Wal
     bool ok = true;
     if (P < 0) {
       ok = false;
-      if (lane == 0) set_status(p.status, TV_DEV_BAD_PREFIX);
+      if (lane == 0 && lead) set_status(p.status, TV_DEV_BAD_PREFIX);
     } else if ((int64_t)P + k + 1 > p.capacity) {
       ok = false;
-      if (lane == 0) set_status(p.status, TV_DEV_CAPACITY);
+      if (lane == 0 && lead) set_status(p.status, TV_DEV_CAPACITY);
     } else if (p.paged) {
       bool page_bad = false;
 #pragma unroll
@@ -554,92 +653,78 @@ __device__ void walk_finish(const AcceptParams& p, int b, WalkSmem& s, const Wal
       }
       if (__any_sync(all, page_bad)) {
         ok = false;
-        if (lane == 0) set_status(p.status, TV_DEV_BAD_PAGE);
+        if (lane == 0 && lead) set_status(p.status, TV_DEV_BAD_PAGE);
       }
     }
     if (lane == 0) {
-      p.accept_len[b] = k;
+      if (lead) p.accept_len[b] = k;
       s.k = k;
       s.ok = ok ? 1 : 0;
     }
   }
   __syncthreads();
   if (!s.ok) return;
-  const int k = s.k;
-  // copy k+1 rows x Hkv heads of K and of V: one thread per row writes the
-  // row's source and destination into a table, then the block moves 16-byte
-  // units (unit u of the list: row u / units_row), up to 8 loads in flight
-  // per thread, all issued before the stores
-  const int64_t row_bytes = (int64_t)p.d * p.esize;
-  const int units_row = (int)(row_bytes / 16);      // a power of two (16 .. 128)
-  const int ushift = __ffs(units_row) - 1;
-  const int kh = (k + 1) * p.Hkv, nrow = 2 * kh;
-  for (int c0 = 0; c0 < nrow; c0 += kCommitRows) {
-    const int cn = min(kCommitRows, nrow - c0);
-    for (int r = tid; r < cn; r += blockDim.x) {
-      const int rr = c0 + r;
-      const int kind = rr / kh, rem = rr - kind * kh, t = rem / p.Hkv, g = rem - t * p.Hkv;
-      const int64_t pos = (int64_t)P + t;
-      int64_t drow;
-      if (p.paged) {
-        const int pid = s.pid[(P + t) / kPageSize - P / kPageSize];
-        drow = ((int64_t)pid * p.Hkv + g) * kPageSize + pos % kPageSize;
-      } else {
-        drow = ((int64_t)b * p.Hkv + g) * p.capacity + pos;
-      }
-      s.src[r] = reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(kind ? p.v_tree : p.k_tree) +
-                                                ((int64_t)g * p.R + o0 + s.path[t]) * row_bytes);
-      s.dst[r] = reinterpret_cast<uint4*>(reinterpret_cast<char*>(kind ? p.v_cache : p.k_cache) + drow * row_bytes);
+  if (stage) {
+    // the staging copies have landed (bounded: on a timeout nothing is committed)
+    const bool in = mbar_wait(smem_u32(&s.staged), 0, &s.abort_flag, kWalkWaitNs);
+    if (!__syncthreads_and(in)) {
+      if (tid == 0) set_status(p.status, TV_DEV_TIMEOUT);
+      s.ok = 0;                                     // read only after the cluster barrier's wait below
+      return;
     }
-    __syncthreads();
-    constexpr int U = 8;
-    const int total = cn * units_row;
-    for (int base = 0; base < total; base += U * (int)blockDim.x) {
-      uint4 v[U];
-#pragma unroll
-      for (int q = 0; q < U; ++q) {
-        const int u = base + q * (int)blockDim.x + tid;
-        if (u < total) v[q] = s.src[u >> ushift][u & (units_row - 1)];
-      }
-#pragma unroll
-      for (int q = 0; q < U; ++q) {
-        const int u = base + q * (int)blockDim.x + tid;
-        if (u < total) s.dst[u >> ushift][u & (units_row - 1)] = v[q];
-      }
-    }
-    __syncthreads();
   }
-  if (tid == 0) p.prefix_len[b] = P + k + 1;
+  walk_commit_rows(p, b, s, stage, o0, P, s.k);
 }
 
-// Walk and commit, one block per sequence.  After the pass kernel of the
-// same call (which writes only the chunk partials and waited for its own
-// predecessor before letting this kernel start), the sequence's lengths,
-// parents, drafts and page ids are read and the ancestors built before the
-// dependency wait; on a given argmax (no pass kernel), everything it reads
-// may come from the kernel just before it, so it waits first.
+// Walk and commit: grid (C, B), clusters of C blocks (one cluster per
+// sequence).  After the pass kernel of the same call (which writes only the
+// chunk partials and waited for its own predecessor before letting this
+// kernel start), the sequence's lengths, parents, drafts, page ids and tree
+// rows are read and the ancestors built before the dependency wait; on a
+// given argmax (no pass kernel), everything it reads may come from the
+// kernel just before it, so it waits first.
 __global__ __launch_bounds__(kWalkThreads) void walk_commit_kernel(AcceptParams p) {
   __shared__ WalkSmem s;
+  extern __shared__ __align__(128) char stage_mem[];
+  char* stage = p.stage_bytes > 0 ? stage_mem : nullptr;
   if (p.given_argmax) {
     dep_wait();
     dep_launch();
   }
-  const int b = blockIdx.x;
+  const int b = blockIdx.y, tid = threadIdx.x;
+  const bool lead = blockIdx.x == 0;
   int o0 = 0, n = 0;
   const bool valid = seq_rows(p.node_offsets, b, p.R, p.max_nodes, nullptr, &o0, &n);
   const int P = valid ? p.prefix_len[b] : 0;
-  if (valid) walk_stage(p, b, s, o0, n, P);
+  if (tid == 0) {
+    s.abort_flag = 0;
+    s.ok = 0;
+    if (stage) {
+      mbar_init(smem_u32(&s.staged), 1);
+      fence_barrier_init();
+    }
+  }
+  if (valid) {
+    walk_stage(p, b, s, o0, n, P);
+    if (stage) walk_stage_rows(p, s, stage, o0, n);
+  }
   WalkRegs wr;
   walk_tree(s, wr, valid ? n : 0);
+  cluster_arrive_release();                         // this block has read prefix_len[b]
   if (!p.given_argmax) {
     dep_wait();
     dep_launch();
   }
   if (!valid) {
-    walk_invalid(p, b);
-    return;
+    if (lead) walk_invalid(p, b);
+  } else {
+    walk_finish(p, b, s, wr, stage, o0, n, P);
   }
-  walk_finish(p, b, s, wr, o0, n, P);
+  // no block exits with its staging copies in flight (they completed before
+  // any commit; this covers the sequences that commit nothing)
+  if (stage && valid && tid == 0) mbar_wait(smem_u32(&s.staged), 0, &s.abort_flag, kWalkWaitNs);
+  cluster_wait_acquire();                           // every block has read prefix_len[b]
+  if (lead && tid == 0 && valid && s.ok) p.prefix_len[b] = P + s.k + 1;
 }
 
 }  // namespace
@@ -658,7 +743,26 @@ cudaError_t launch_accept_commit(const AcceptParams& p, cudaStream_t s) {
                                grid, dim3(256), 0, s, p);
     if (e != cudaSuccess) return e;
   }
-  return launch_dep(walk_commit_kernel, dim3(p.B), dim3(kWalkThreads), 0, s, p);
+  const int C = walk_cluster(p.Hkv);
+  if (p.stage_bytes > 48 * 1024) {
+    const cudaError_t e = ensure_max_dynamic_smem<walk_commit_kernel>(p.stage_bytes);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C, p.B);
+  cfg.blockDim = dim3(kWalkThreads);
+  cfg.dynamicSmemBytes = (size_t)p.stage_bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = C;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, walk_commit_kernel, p);
 }
 
 }  // namespace tv

@@ -325,6 +325,7 @@ int accept_commit_impl(const tv_desc* desc, int32_t vocab, int32_t logits_dtype,
   a.B = desc->batch; a.R = desc->total_rows; a.Hkv = desc->num_kv_heads; a.d = desc->head_dim;
   a.esize = desc->dtype == TV_BF16 ? 2 : 4; a.max_nodes = desc->max_nodes; a.paged = desc->page_size != 0;
   a.capacity = desc->capacity; a.num_pages = desc->num_pages; a.max_pages = desc->capacity / kPageSize;
+  a.stage_bytes = walk_stage_bytes(a.Hkv, a.max_nodes, (int64_t)a.d * a.esize);
   cudaError_t e = launch_accept_commit(a, as_stream(stream));
   return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
 }
@@ -514,6 +515,7 @@ int tree_accept_commit_argmax(const tv_desc* desc, const int32_t* d_argmax, cons
   a.B = desc->batch; a.R = desc->total_rows; a.Hkv = desc->num_kv_heads; a.d = desc->head_dim;
   a.esize = desc->dtype == TV_BF16 ? 2 : 4; a.max_nodes = desc->max_nodes; a.paged = desc->page_size != 0;
   a.capacity = desc->capacity; a.num_pages = desc->num_pages; a.max_pages = desc->capacity / kPageSize;
+  a.stage_bytes = walk_stage_bytes(a.Hkv, a.max_nodes, (int64_t)a.d * a.esize);
   cudaError_t e = launch_accept_commit(a, as_stream(stream));
   return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
 }

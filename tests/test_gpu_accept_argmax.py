@@ -74,3 +74,32 @@ def test_lm_head_argmax_feeds_the_walk():
     assert int(lm.status[0]) == 0
     assert np.array_equal(lm.argmax.cpu().numpy(), am_ref)
     check_walk_commit(w, st, am_ref)
+
+
+# Shapes of the walk's cluster (one block per (K or V, KV head) set, at most 8
+# blocks, extra sets shared round-robin) and of its two commit sources: tree
+# rows staged in shared memory when a block's sets fit the 160 KB budget,
+# else read from the tree buffers.
+@pytest.mark.parametrize("hq,hkv,d,dtype,paged", [
+    (3, 1, 256, "bf16", False),    # a cluster of 2 blocks
+    (6, 3, 128, "bf16", True),     # 6 blocks, paged cache
+    (10, 5, 128, "bf16", False),   # 8 blocks, blocks 0 and 1 hold two sets
+    (10, 5, 512, "f32", False),    # two 2 KB-row sets per block: copied from the tree buffers
+])
+def test_walk_cluster_shapes(hq, hkv, d, dtype, paged):
+    spec = wl.small_variant(5, hq=hq, hkv=hkv, d=d, dtype=dtype, logit_dtype=dtype, paged=paged, batch=3,
+                            prefix=(40, 300), vocab=2003, seed=77 + hkv + d)
+    w = workload(spec)
+    sets_per_block = -(-2 * hkv // min(8, 2 * hkv))
+    staged = sets_per_block * w.max_nodes * d * (2 if dtype == "bf16" else 4) <= 160 * 1024
+    assert staged == (d != 512)                            # each commit source is covered
+    am = oracle.argmax_rows(w.logits)
+    st = DeviceStep(w)
+    st.accept_commit()                                     # the argmax pass, then the walk
+    torch.cuda.synchronize()
+    assert np.array_equal(st.argmax.cpu().numpy(), am)
+    check_walk_commit(w, st, am)
+    st = DeviceStep(w)
+    st.accept_commit_argmax(torch.from_numpy(am).to(torch.int32).cuda())
+    torch.cuda.synchronize()
+    check_walk_commit(w, st, am)
