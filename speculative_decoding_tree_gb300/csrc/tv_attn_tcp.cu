@@ -566,80 +566,85 @@ tv_attn_tcp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         anc = row_ok ? p.anc[qe->o0 + (m0 + r) / G] : 0ull;
       }
       float m_ref = -INFINITY, l = 0.f;
+      const bool warp_live = __any_sync(kAll, row_ok);
       for (int t = 0; t < T && ok; ++t) {
         const int tg = tt + t;
         if (!__all_sync(kAll, mbar_wait(S_FULL(tg & 1), (tg >> 1) & 1, abort_flag, kWaitNs))) { ok = false; break; }
         tc_fence_after();
         const uint32_t sbuf = tmem + lane_base + (uint32_t)((tg & 1) * 128);
-        float sv[BN / 2];
-        {
-          uint32_t rr[64];
-          tmem_ld_x64(sbuf + kofs, rr);
-#pragma unroll
-          for (int e = 0; e < 64; ++e) sv[e] = __uint_as_float(rr[e]);
-        }
-        const bool tree = (t == npt);
-        const bool partial = tree || (t == npt - 1 && tail_valid < BN);
-        if (partial) {
-          // tree tile: ancestor bits; last prefix tile: key range
-          const int lim = tree ? min(n, 64) : tail_valid;
-#pragma unroll
-          for (int e = 0; e < 64; ++e) {
-            const int key = kofs + e;
-            bool vis = key < lim;
-            if (tree) vis = vis && ((anc >> (key & 63)) & 1ull);
-            sv[e] = vis ? sv[e] : -INFINITY;
+        // a warp whose 32 rows all lie past the tree's rows leaves P as it is:
+        // the products of those rows are never read
+        if (warp_live) {
+          float sv[BN / 2];
+          {
+            uint32_t rr[64];
+            tmem_ld_x64(sbuf + kofs, rr);
+  #pragma unroll
+            for (int e = 0; e < 64; ++e) sv[e] = __uint_as_float(rr[e]);
           }
-        }
-        float mq[4] = {sv[0], sv[1], sv[2], sv[3]};
-#pragma unroll
-        for (int e = 4; e < 64; e += 2) mq[(e >> 1) & 3] = fmax3(mq[(e >> 1) & 3], sv[e], sv[e + 1]);
-        const float mx = fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
-        const float m_tile = mx == -INFINITY ? -INFINITY : mx * c2;
-        const float m_new = fmaxf(m_ref, m_tile);
-        const bool first = (m_ref == -INFINITY);
-        const bool need = !first && (m_new > m_ref + kRescaleThreshold);
-        if (__any_sync(kAll, need)) {
-          // this half's O rows must hold P(t-1) V(t-1) before they are rescaled (t >= 1 here)
-          const int ug = tg - 1;
-          if (!__all_sync(kAll, mbar_wait(O_DONE(half, ug & 1), (ug >> 1) & 1, abort_flag, kWaitNs))) {
-            ok = false;
-            break;
+          const bool tree = (t == npt);
+          const bool partial = tree || (t == npt - 1 && tail_valid < BN);
+          if (partial) {
+            // tree tile: ancestor bits; last prefix tile: key range
+            const int lim = tree ? min(n, 64) : tail_valid;
+  #pragma unroll
+            for (int e = 0; e < 64; ++e) {
+              const int key = kofs + e;
+              bool vis = key < lim;
+              if (tree) vis = vis && ((anc >> (key & 63)) & 1ull);
+              sv[e] = vis ? sv[e] : -INFINITY;
+            }
           }
-          tc_fence_after();
-          const float alpha = need ? ex2(m_ref - m_new) : 1.f;
-#pragma unroll 1
-          for (int c = 0; c < D; c += 32) {
-            uint32_t rr[32];
-            tmem_ld_x32(obuf + c, rr);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
-            tmem_st_x32(obuf + c, rr);
+          float mq[4] = {sv[0], sv[1], sv[2], sv[3]};
+  #pragma unroll
+          for (int e = 4; e < 64; e += 2) mq[(e >> 1) & 3] = fmax3(mq[(e >> 1) & 3], sv[e], sv[e + 1]);
+          const float mx = fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
+          const float m_tile = mx == -INFINITY ? -INFINITY : mx * c2;
+          const float m_new = fmaxf(m_ref, m_tile);
+          const bool first = (m_ref == -INFINITY);
+          const bool need = !first && (m_new > m_ref + kRescaleThreshold);
+          if (__any_sync(kAll, need)) {
+            // this half's O rows must hold P(t-1) V(t-1) before they are rescaled (t >= 1 here)
+            const int ug = tg - 1;
+            if (!__all_sync(kAll, mbar_wait(O_DONE(half, ug & 1), (ug >> 1) & 1, abort_flag, kWaitNs))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const float alpha = need ? ex2(m_ref - m_new) : 1.f;
+  #pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+              uint32_t rr[32];
+              tmem_ld_x32(obuf + c, rr);
+  #pragma unroll
+              for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
+              tmem_st_x32(obuf + c, rr);
+            }
+            if (need) {
+              l *= alpha;
+              m_ref = m_new;
+            }
           }
-          if (need) {
-            l *= alpha;
-            m_ref = m_new;
+          if (first) m_ref = m_new;
+          const float nm = m_ref == -INFINITY ? 0.f : -m_ref;   // masked keys: 2^-inf = 0
+          // P = 2^(s c2 - m) in packed pairs (f32x2 products and sums)
+          const uint64_t c2x2 = pk2(c2, c2), nmx2 = pk2(nm, nm);
+          uint64_t l4[4] = {0ull, 0ull, 0ull, 0ull};   // packed (+0, +0)
+          uint32_t pk[32];
+  #pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float2 x = up2(ffma2(pk2(sv[2 * e], sv[2 * e + 1]), c2x2, nmx2));
+            const uint64_t y = pk2(ex2(x.x), ex2(x.y));
+            l4[e & 3] = fadd2(l4[e & 3], y);
+            const float2 yf = up2(y);
+            pk[e] = pack_bf16(yf.x, yf.y);
           }
+          {
+            const float2 la = up2(fadd2(fadd2(l4[0], l4[1]), fadd2(l4[2], l4[3])));
+            l += la.x + la.y;
+          }
+          tmem_st_x32(sbuf + half * 32, pk);          // P over the S columns, bf16 pairs
         }
-        if (first) m_ref = m_new;
-        const float nm = m_ref == -INFINITY ? 0.f : -m_ref;   // masked keys: 2^-inf = 0
-        // P = 2^(s c2 - m) in packed pairs (f32x2 products and sums)
-        const uint64_t c2x2 = pk2(c2, c2), nmx2 = pk2(nm, nm);
-        uint64_t l4[4] = {0ull, 0ull, 0ull, 0ull};   // packed (+0, +0)
-        uint32_t pk[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float2 x = up2(ffma2(pk2(sv[2 * e], sv[2 * e + 1]), c2x2, nmx2));
-          const uint64_t y = pk2(ex2(x.x), ex2(x.y));
-          l4[e & 3] = fadd2(l4[e & 3], y);
-          const float2 yf = up2(y);
-          pk[e] = pack_bf16(yf.x, yf.y);
-        }
-        {
-          const float2 la = up2(fadd2(fadd2(l4[0], l4[1]), fadd2(l4[2], l4[3])));
-          l += la.x + la.y;
-        }
-        tmem_st_x32(sbuf + half * 32, pk);          // P over the S columns, bf16 pairs
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(P_FULL(half, tg & 1));
