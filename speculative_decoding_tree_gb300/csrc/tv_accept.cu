@@ -721,8 +721,12 @@ __global__ __launch_bounds__(kWalkThreads) void walk_commit_kernel(AcceptParams 
     walk_finish(p, b, s, wr, stage, o0, n, P);
   }
   // no block exits with its staging copies in flight (they completed before
-  // any commit; this covers the sequences that commit nothing)
-  if (stage && valid && tid == 0) mbar_wait(smem_u32(&s.staged), 0, &s.abort_flag, kWalkWaitNs);
+  // any commit; this covers the sequences that commit nothing, and a wait
+  // that gave up: its own flag is raised, so this wait has a fresh one)
+  if (stage && valid && tid == 0) {
+    int spare = 0;
+    mbar_wait(smem_u32(&s.staged), 0, &spare, kWalkWaitNs);
+  }
   cluster_wait_acquire();                           // every block has read prefix_len[b]
   if (lead && tid == 0 && valid && s.ok) p.prefix_len[b] = P + s.k + 1;
 }
